@@ -1,0 +1,194 @@
+/*
+ * trtv.h -- C ABI of the GB300 (sm_103a) verify-attention library.
+ *
+ * Multi-token speculative-decoding verify attention over a paged KV cache:
+ * every request carries qo_len = 1 + draft_len query tokens; token t attends
+ * positions p <= kv_len - qo_len + t of its request (the causal "ladder":
+ * token t sees kv_len - qo_len + t + 1 positions).  Sources, by page title
+ * and section:
+ *   "Eagle3 for M3 MSA path + CUDA graphs compatibility" (fork PR #3),
+ *     commit "... verify": the ladder, the proxy (OnlyScore) pass, top-k
+ *     clipped to per-token ladder valid-page counts, sparse GQA attention;
+ *     CUDA-graphs commit: device-only planning, prepare-time buffers, stable
+ *     pointers, kv_lens mutated on device between replays, no allocation
+ *     while capturing.
+ *   "wrap up eagle changes in m3 side branch" (TensorRT-LLM #18066):
+ *     MiniMaxM3DraftKVCacheView commit (slot s's K page at s * stride, V page
+ *     at s * stride + 1; kv_offset == 1; P128 pages) and
+ *     copy_batch_block_offsets commit (padded entries address slot 0).
+ *   "Default Minimax-m3 to unified draft-target kv manager" (#17835),
+ *     "Grouped-HND draft KV transfer": a P128 page is consumed as four
+ *     head-major 32-token groups, [group=4, local_head, 32, head_dim].
+ *
+ * ---- Data layout (all device memory, owned by the caller) ----------------
+ *   q          bf16  [batch * qo_len, num_q_heads, head_dim]; row = b*qo_len + t
+ *   kv_pool    page buffers, each [4][num_kv_heads][32][head_dim] elements of
+ *              kv_dtype (bf16: 2 bytes, FP8 E4M3: 1 byte).  Slot s owns
+ *              buffers s*slot_stride .. s*slot_stride + slot_stride - 1; this
+ *              layer's K page is buffer s*slot_stride, its V page the next one.
+ *              Position p of a request lives in slot page_table[b][p / 128],
+ *              group (p % 128) / 32, row p % 32 of its head.  The pool holds
+ *              num_slots * slot_stride buffers; its address must be 16-byte
+ *              aligned.
+ *   page_table int32 [batch, max_pages_per_req]; entries past a request's
+ *              pages are ignored (conventionally 0).
+ *   kv_lens    int32 [batch], read on the device at run time (may change
+ *              between launches or CUDA-graph replays; never read on the host).
+ *   out        [batch * qo_len, num_q_heads, head_dim] bf16 or f32.
+ *   query head hq reads KV head hq / (num_q_heads / num_kv_heads).
+ *
+ * ---- Conventions ---------------------------------------------------------
+ *   - Every entry point only validates arguments on the host and enqueues
+ *     kernels on `stream` (a cudaStream_t; NULL = legacy default stream).  It
+ *     never allocates, never synchronises and never reads device memory, so
+ *     it may be captured into a CUDA graph; grids are sized from batch,
+ *     heads and max_pages_per_req, never from kv_lens.
+ *   - Returns TRTV_ERR_INVALID_ARG for inconsistent geometry or NULL
+ *     pointers, TRTV_ERR_UNSUPPORTED for valid geometry outside what the
+ *     kernels handle, TRTV_ERR_WORKSPACE when ws_bytes is too small, and
+ *     TRTV_ERR_CUDA when a launch fails.  Nothing is enqueued on error.
+ *   - Data errors are found on the device (kv_len < qo_len or beyond
+ *     128 * max_pages_per_req; a used page id outside [0, num_slots); a
+ *     top-k block index >= max_pages_per_req).  Affected output rows are
+ *     zero (or, for a bad page id, finite but meaningless), no kernel traps,
+ *     and a bit is set in a per-device error word read by
+ *     trtv_get_device_error.
+ *   - Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef TRTV_H_
+#define TRTV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TRTV_OK = 0,
+  TRTV_ERR_INVALID_ARG = 1,
+  TRTV_ERR_UNSUPPORTED = 2,
+  TRTV_ERR_CUDA = 3,
+  TRTV_ERR_WORKSPACE = 4
+} trtv_status;
+
+typedef enum { TRTV_BF16 = 0, TRTV_FP8_E4M3 = 1, TRTV_F32 = 2 } trtv_dtype;
+
+/* Device error word bits (trtv_get_device_error). */
+#define TRTV_DEVERR_KV_LEN 1    /* kv_len < qo_len or kv_len > 128 * max_pages */
+#define TRTV_DEVERR_PAGE_ID 2   /* a used page-table entry outside [0, num_slots) */
+#define TRTV_DEVERR_BLOCK_IDX 4 /* a top-k block index >= max_pages_per_req */
+
+typedef struct {
+  int32_t batch;             /* requests B >= 1 */
+  int32_t qo_len;            /* T = 1 + draft_len, 1 <= T <= 32 */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hk, Hq % Hk == 0 */
+  int32_t head_dim;          /* D: 64 or 128 */
+  int32_t max_pages_per_req; /* page-table row pitch (capacity / 128) */
+  int32_t num_slots;         /* slots in the pool; page ids must be < num_slots */
+  int32_t slot_stride;       /* page buffers per slot, >= 2 (V = K + 1: kv_offset == 1) */
+  int32_t kv_dtype;          /* TRTV_BF16 or TRTV_FP8_E4M3 */
+  float sm_scale;            /* softmax scale, e.g. 1 / sqrt(D) */
+  float k_scale;             /* per-tensor dequantisation scale of K (1 for bf16) */
+  float v_scale;             /* per-tensor dequantisation scale of V (1 for bf16) */
+  int32_t num_ctas;          /* work CTAs of the attention / proxy kernels;
+                                0 = one per SM (results do not depend on it
+                                beyond fp32 rounding) */
+} trtv_geom;
+
+/* Human-readable name of a status code (static storage). */
+const char* trtv_status_string(trtv_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t trtv_version(void);
+
+/*
+ * P32 sub-page view of the P128 pages (sources: #18066 view and padding
+ * commits; #17835 "Grouped-HND draft KV transfer").
+ * For every request b and logical 32-token block j < 4 * max_pages_per_req:
+ *   s = page_table[b][j / 4] if j < ceil(kv_len[b] / 32), else 0 (padding
+ *       addresses slot 0's memory);
+ *   k_sub[b][j] = 4 * (s * slot_stride) + j % 4;
+ *   v_sub[b][j] = 4 * (s * slot_stride + 1) + j % 4;
+ * in units of one [num_kv_heads, 32, head_dim] sub-page of the pool.
+ * k_sub, v_sub: int32 [batch, 4 * max_pages_per_req] device outputs.
+ * Requests with bad lengths or page ids still get entries by the same rule
+ * and raise the device error word.
+ */
+trtv_status trtv_subpage_view(const trtv_geom* geom, const int32_t* page_table,
+                              const int32_t* kv_lens, int32_t* k_sub, int32_t* v_sub,
+                              void* stream);
+
+/*
+ * Workspace bytes that trtv_verify_dense and trtv_msa_sparse_attn need for
+ * this geometry (topk = the sparse path's k, 0 for dense only).  The
+ * workspace is caller-allocated device memory, 256-byte aligned, reusable
+ * across calls (no initialisation needed); 0 on invalid geometry.
+ */
+size_t trtv_workspace_bytes(const trtv_geom* geom, int32_t topk);
+
+/*
+ * Dense ladder verify attention (source: PR #3 "... verify" commit; dense
+ * layers' ladder SDPA mask, identical to decode at qo_len = 1).
+ * out[b*T + t][hq][:] = sum_{p <= L_b - T + t} softmax_p(x) v_p, with
+ *   x_p = sm_scale * k_scale * (q[b*T + t][hq] . k_p),  v_p scaled by v_scale,
+ * k_p / v_p from KV head hq / G of request b.  Split-KV across CTAs with a
+ * log-sum-exp combine; fp32 accumulation.  out_dtype: TRTV_BF16 or TRTV_F32.
+ */
+trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* kv_pool,
+                              const int32_t* page_table, const int32_t* kv_lens, void* out,
+                              int32_t out_dtype, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * MSA proxy (OnlyScore) block scores (source: PR #3 "... verify" commit:
+ * natively multi-token, inclusive causal bound with offset kv_len - qo_len).
+ * scores[b][t][h][j] (fp32 [batch, qo_len, num_kv_heads, max_pages_per_req])
+ * = max over the G query heads of KV head h and over positions p of 128-token
+ * page j with p <= L_b - T + t of sm_scale * k_scale * (q . k_p); -inf for
+ * pages past the bound or past the request's pages, and for every page of an
+ * invalid request.  Requires G <= 16.
+ */
+trtv_status trtv_msa_proxy_score(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                 const int32_t* page_table, const int32_t* kv_lens,
+                                 float* scores, void* stream);
+
+/*
+ * Per-token top-k block selection (source: PR #3 "... verify" commit: top-k
+ * gets per-token ladder valid-page counts).  For each (b, t, h): of the
+ * n_t = floor((L_b - T + t) / 128) + 1 blocks the token can see, keep the
+ * min(topk, n_t) with the largest score, ties to the lower block index;
+ * block_idx[b][t][h][0..topk) lists them in ascending order, padded with -1
+ * (all -1 for an invalid request).  block_idx: int32 [B, T, Hk, topk].
+ * 1 <= topk <= 1024; max_pages_per_req <= 16384.
+ */
+trtv_status trtv_msa_topk(const trtv_geom* geom, const float* scores, const int32_t* kv_lens,
+                          int32_t topk, int32_t* block_idx, void* stream);
+
+/*
+ * Sparse GQA attention over the selected blocks (source: PR #3 "... verify"
+ * commit).  As trtv_verify_dense, with token t of request b attending only
+ * positions inside the blocks block_idx[b][t][h][0..topk) (entries < 0 are
+ * ignored, repeated entries count once) and within its ladder bound.  Each
+ * selected block is read once per (request, KV head) however many of the
+ * request's tokens selected it.  A row with no visible position is zero.
+ */
+trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                 const int32_t* page_table, const int32_t* kv_lens,
+                                 const int32_t* block_idx, int32_t topk, void* out,
+                                 int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/*
+ * Read and clear the current device's error word (TRTV_DEVERR_* bits).
+ * Synchronises `stream`; not for use while capturing a graph.
+ */
+trtv_status trtv_get_device_error(int32_t* host_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRTV_H_ */

@@ -1,0 +1,179 @@
+"""Python binding of the GB300 verify-attention library (``include/trtv.h``).
+
+Argument marshalling only: each function takes torch CUDA tensors (or raw
+device pointers), converts them to pointers and sizes, and calls the C entry
+point of the same name in ``_lib/libtrtv.so``.  Every step of the path runs in
+the library's CUDA kernels; there is no fallback.  Importing the package does
+not need a GPU, but calling a compute function without the built library or
+without a GPU raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+__all__ = [
+    "TRTV_OK", "TRTV_BF16", "TRTV_FP8_E4M3", "TRTV_F32", "TrtvError", "Geom", "load",
+    "trtv_subpage_view", "trtv_workspace_bytes", "trtv_verify_dense", "trtv_msa_proxy_score",
+    "trtv_msa_topk", "trtv_msa_sparse_attn", "trtv_get_device_error", "trtv_version",
+    "trtv_status_string", "geom_of", "EXPORTS",
+]
+
+TRTV_OK, TRTV_ERR_INVALID_ARG, TRTV_ERR_UNSUPPORTED, TRTV_ERR_CUDA, TRTV_ERR_WORKSPACE = range(5)
+TRTV_BF16, TRTV_FP8_E4M3, TRTV_F32 = 0, 1, 2
+DEVERR_KV_LEN, DEVERR_PAGE_ID, DEVERR_BLOCK_IDX, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+# every function the C header declares
+EXPORTS = ("trtv_status_string", "trtv_version", "trtv_subpage_view", "trtv_workspace_bytes",
+           "trtv_verify_dense", "trtv_msa_proxy_score", "trtv_msa_topk", "trtv_msa_sparse_attn",
+           "trtv_get_device_error")
+
+
+class TrtvError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class Geom(ctypes.Structure):
+    """Mirror of ``trtv_geom``."""
+    _fields_ = [("batch", ctypes.c_int32), ("qo_len", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_pages_per_req", ctypes.c_int32),
+                ("num_slots", ctypes.c_int32), ("slot_stride", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("sm_scale", ctypes.c_float),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("num_ctas", ctypes.c_int32)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load ``libtrtv.so`` (building it first when asked).  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"libtrtv.so is not built ({path}); run __graft_entry__.build() "
+                              "or python -m speculative_decode_verify_kv_gb300._build")
+        _build.build()
+    h = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    G = ctypes.POINTER(Geom)
+    h.trtv_status_string.restype = ctypes.c_char_p
+    h.trtv_status_string.argtypes = [ctypes.c_int]
+    h.trtv_version.restype = i32
+    h.trtv_version.argtypes = []
+    h.trtv_subpage_view.restype = ctypes.c_int
+    h.trtv_subpage_view.argtypes = [G, vp, vp, vp, vp, vp]
+    h.trtv_workspace_bytes.restype = sz
+    h.trtv_workspace_bytes.argtypes = [G, i32]
+    h.trtv_verify_dense.restype = ctypes.c_int
+    h.trtv_verify_dense.argtypes = [G, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+    h.trtv_msa_proxy_score.restype = ctypes.c_int
+    h.trtv_msa_proxy_score.argtypes = [G, vp, vp, vp, vp, vp, vp]
+    h.trtv_msa_topk.restype = ctypes.c_int
+    h.trtv_msa_topk.argtypes = [G, vp, vp, i32, vp, vp]
+    h.trtv_msa_sparse_attn.restype = ctypes.c_int
+    h.trtv_msa_sparse_attn.argtypes = [G, vp, vp, vp, vp, vp, i32, vp, i32, vp, sz, vp]
+    h.trtv_get_device_error.restype = ctypes.c_int
+    h.trtv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+    _lib = h
+    return h
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int) -> None:
+    if st != TRTV_OK:
+        raise TrtvError(fn, st, load().trtv_status_string(st).decode())
+
+
+def geom_of(p, num_ctas: int = 0, **over) -> Geom:
+    """Geom from a workloads.VerifyProblem-like object (fields overridable)."""
+    f = dict(batch=p.batch, qo_len=p.qo_len, num_q_heads=p.num_q_heads,
+             num_kv_heads=p.num_kv_heads, head_dim=p.head_dim,
+             max_pages_per_req=p.max_pages_per_req, num_slots=p.num_slots,
+             slot_stride=p.slot_stride,
+             kv_dtype=TRTV_FP8_E4M3 if p.kv_dtype == "fp8_e4m3" else TRTV_BF16,
+             sm_scale=p.sm_scale, k_scale=p.k_scale, v_scale=p.v_scale, num_ctas=num_ctas)
+    f.update(over)
+    return Geom(**f)
+
+
+def trtv_version() -> int:
+    return load().trtv_version()
+
+
+def trtv_status_string(st: int) -> str:
+    return load().trtv_status_string(st).decode()
+
+
+def trtv_workspace_bytes(geom: Geom, topk: int = 0) -> int:
+    return load().trtv_workspace_bytes(ctypes.byref(geom), topk)
+
+
+def trtv_subpage_view(geom: Geom, page_table, kv_lens, k_sub, v_sub, stream=None) -> None:
+    _check("trtv_subpage_view", load().trtv_subpage_view(
+        ctypes.byref(geom), _ptr(page_table), _ptr(kv_lens), _ptr(k_sub), _ptr(v_sub),
+        _stream(stream)))
+
+
+def trtv_verify_dense(geom: Geom, q, kv_pool, page_table, kv_lens, out, out_dtype: int,
+                      workspace, ws_bytes: int, stream=None) -> None:
+    _check("trtv_verify_dense", load().trtv_verify_dense(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens), _ptr(out),
+        out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_msa_proxy_score(geom: Geom, q, kv_pool, page_table, kv_lens, scores, stream=None) -> None:
+    _check("trtv_msa_proxy_score", load().trtv_msa_proxy_score(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens),
+        _ptr(scores), _stream(stream)))
+
+
+def trtv_msa_topk(geom: Geom, scores, kv_lens, topk: int, block_idx, stream=None) -> None:
+    _check("trtv_msa_topk", load().trtv_msa_topk(
+        ctypes.byref(geom), _ptr(scores), _ptr(kv_lens), topk, _ptr(block_idx), _stream(stream)))
+
+
+def trtv_msa_sparse_attn(geom: Geom, q, kv_pool, page_table, kv_lens, block_idx, topk: int, out,
+                         out_dtype: int, workspace, ws_bytes: int, stream=None) -> None:
+    _check("trtv_msa_sparse_attn", load().trtv_msa_sparse_attn(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens),
+        _ptr(block_idx), topk, _ptr(out), out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_get_device_error(stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("trtv_get_device_error", load().trtv_get_device_error(ctypes.byref(v), _stream(stream)))
+    return v.value

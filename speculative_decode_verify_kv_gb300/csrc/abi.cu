@@ -1,0 +1,467 @@
+// abi.cu -- the extern "C" entry points declared in include/trtv.h: argument
+// validation, workspace and shared-memory planning, TMA descriptor encoding
+// and kernel launches.  Host code only; it never allocates device memory,
+// never synchronises (except trtv_get_device_error) and never reads device
+// data, so every compute entry point can be captured into a CUDA graph.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "common.cuh"
+#include "launch.h"
+
+// Per-device error word (TRTV_DEVERR_* bits), set by the kernels.
+__device__ int g_trtv_device_error;
+
+namespace trtv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kSmemOptin = 232448;  // opt-in shared memory per block on sm_103
+constexpr size_t kAlignSlack = 1024;
+
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+int* g_err_ptr[kMaxDevices];
+std::set<std::pair<const void*, int>> g_smem_set;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sm_count[d] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    g_sm_count[d] = n;
+  }
+  return g_sm_count[d];
+}
+
+int* err_word() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_trtv_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<int*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Derived shape of one call.
+struct Plan {
+  int group, group_pad, rows, mt, rows_pad, num_ctas, n_seq;
+  int64_t pool_rows;
+  // workspace
+  size_t ws_o, ws_lse, ws_blocks, ws_masks, ws_count, ws_total;
+  int plan_cap;
+};
+
+trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
+  if (g == nullptr) return TRTV_ERR_INVALID_ARG;
+  if (g->batch < 1 || g->qo_len < 1 || g->num_q_heads < 1 || g->num_kv_heads < 1 ||
+      g->num_q_heads % g->num_kv_heads != 0 || g->max_pages_per_req < 1 || g->num_slots < 1 ||
+      g->slot_stride < 2 || g->num_ctas < 0)
+    return TRTV_ERR_INVALID_ARG;
+  if (g->kv_dtype != TRTV_BF16 && g->kv_dtype != TRTV_FP8_E4M3) return TRTV_ERR_INVALID_ARG;
+  if (!(g->sm_scale > 0.f) || !(g->k_scale > 0.f) || !std::isfinite(g->sm_scale) ||
+      !std::isfinite(g->k_scale) || !std::isfinite(g->v_scale))
+    return TRTV_ERR_INVALID_ARG;
+  if (g->head_dim != 64 && g->head_dim != 128) return TRTV_ERR_UNSUPPORTED;
+  if (g->kv_dtype == TRTV_FP8_E4M3 && g->head_dim != 128) return TRTV_ERR_UNSUPPORTED;
+  if (g->qo_len > 32) return TRTV_ERR_UNSUPPORTED;
+  if (topk < 0 || topk > 1024) return TRTV_ERR_INVALID_ARG;
+  Plan p{};
+  p.group = g->num_q_heads / g->num_kv_heads;
+  p.group_pad = p.group <= 16 ? next_pow2(p.group) : (p.group + 15) / 16 * 16;
+  p.rows = p.group_pad * g->qo_len;
+  p.mt = next_pow2((p.rows + 15) / 16);
+  if (p.mt > 8) return TRTV_ERR_UNSUPPORTED;
+  p.rows_pad = 16 * p.mt;
+  p.pool_rows = static_cast<int64_t>(g->num_slots) * g->slot_stride * kGroups * g->num_kv_heads * kSub;
+  if (p.pool_rows >= (int64_t{1} << 31)) return TRTV_ERR_UNSUPPORTED;
+  p.n_seq = g->batch * g->num_kv_heads;
+  if (static_cast<int64_t>(g->batch) * g->num_kv_heads > (1 << 16)) return TRTV_ERR_UNSUPPORTED;
+  int ctas = g->num_ctas > 0 ? g->num_ctas : sm_count();
+  if (ctas <= 0) return TRTV_ERR_CUDA;
+  p.num_ctas = ctas;
+  const size_t P2 = 2 * static_cast<size_t>(ctas);
+  size_t off = 0;
+  p.ws_o = off;
+  off = align_up(off + P2 * p.rows_pad * g->head_dim * sizeof(float), 256);
+  p.ws_lse = off;
+  off = align_up(off + P2 * p.rows_pad * sizeof(float), 256);
+  p.plan_cap = topk > 0 ? std::min(g->qo_len * topk, g->max_pages_per_req) : 0;
+  p.ws_blocks = off;
+  off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(int32_t), 256);
+  p.ws_masks = off;
+  off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(uint32_t), 256);
+  p.ws_count = off;
+  off = align_up(off + (topk > 0 ? static_cast<size_t>(p.n_seq) * sizeof(int32_t) : 0), 256);
+  p.ws_total = off;
+  *pl = p;
+  return TRTV_OK;
+}
+
+bool encode_pool_map(const trtv_geom* g, const Plan& pl, const void* pool, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (enc == nullptr) return false;
+  const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
+  const int elem = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g->head_dim), static_cast<cuuint64_t>(pl.pool_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g->head_dim) * elem};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem), 32};
+  cuuint32_t estr[2] = {1, 1};
+  std::memset(map, 0, sizeof(*map));
+  const CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(pool), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Shared-memory carve-up of the attention kernel; false if it cannot fit.
+bool plan_attn_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
+  const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
+  const int D = g->head_dim;
+  const int NB = fp8 ? 1 : D * 2 / 128;
+  const int nsl = kConsumerWarps / pl.mt;
+  const int half = D / 2 < 64 ? D / 2 : 64;
+  const size_t stage = static_cast<size_t>(2) * kGroups * NB * kBox;
+  const size_t conv = fp8 ? static_cast<size_t>(2) * kGroups * 2 * kBox : 0;
+  const size_t merge = nsl > 1 ? static_cast<size_t>(pl.mt) * 16 * (half + 8) * sizeof(float) : 0;
+  const size_t ml = (kConsumerWarps * 16 * 2 + 128 * 2) * sizeof(float);
+  const int nitems = sparse ? pl.n_seq : g->batch;
+  const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
+  const size_t budget = kSmemOptin - kAlignSlack;
+  const size_t fixed = conv + merge + ml + scan + 2 * 8 * sizeof(uint64_t);
+  if (fixed + 2 * stage > budget) return false;
+  int nst = static_cast<int>((budget - fixed) / stage);
+  if (nst > 4) nst = 4;
+  size_t off = 0;
+  a->off_stage = 0;
+  a->stage_bytes = static_cast<int>(stage);
+  a->off_k = 0;
+  a->off_v = static_cast<int>(stage / 2);
+  off = static_cast<size_t>(nst) * stage;
+  a->off_conv = static_cast<int>(off);
+  off += conv;
+  a->off_merge = static_cast<int>(off);
+  off += merge;
+  a->off_ml = static_cast<int>(off);
+  off += ml;
+  a->off_scan = static_cast<int>(off);
+  off += scan;
+  a->off_bar = static_cast<int>(align_up(off, 8));
+  off = a->off_bar + 2 * nst * sizeof(uint64_t);
+  a->nstages = nst;
+  *bytes = off + kAlignSlack;
+  return *bytes <= kSmemOptin;
+}
+
+bool plan_proxy_smem(const trtv_geom* g, const Plan& pl, ProxyParams* a, size_t* bytes) {
+  const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
+  const int NB = fp8 ? 1 : g->head_dim * 2 / 128;
+  const size_t stage = static_cast<size_t>(kGroups) * NB * kBox;
+  const size_t scan = align_up((static_cast<size_t>(g->batch) + 1 + 32) * sizeof(int32_t), 16);
+  const size_t budget = kSmemOptin - kAlignSlack - 1024;  // 1 KB for static shared memory
+  const size_t per_stage = stage + 8 * 32 * sizeof(float) + 2 * sizeof(uint64_t);
+  if (scan + 2 * per_stage > budget) return false;
+  int nst = static_cast<int>((budget - scan) / per_stage);
+  if (nst > 8) nst = 8;
+  (void)pl;
+  size_t off = 0;
+  a->off_stage = 0;
+  a->stage_bytes = static_cast<int>(stage);
+  off = static_cast<size_t>(nst) * stage;
+  a->off_red = static_cast<int>(off);
+  off += static_cast<size_t>(nst) * 8 * 32 * sizeof(float);
+  a->off_scan = static_cast<int>(off);
+  off += scan;
+  a->off_bar = static_cast<int>(align_up(off, 8));
+  off = a->off_bar + 2 * nst * sizeof(uint64_t);
+  a->nstages = nst;
+  *bytes = off + kAlignSlack;
+  return *bytes <= kSmemOptin - 1024;
+}
+
+trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, const int32_t* pt,
+                        const int32_t* lens, const int32_t* block_idx, int topk, void* out,
+                        int32_t out_dtype, void* ws, size_t ws_bytes, void* stream) {
+  const bool sparse = block_idx != nullptr;
+  Plan pl;
+  trtv_status s = make_plan(g, sparse ? topk : 0, &pl);
+  if (s != TRTV_OK) return s;
+  if (sparse && topk < 1) return TRTV_ERR_INVALID_ARG;
+  if (q == nullptr || pool == nullptr || pt == nullptr || lens == nullptr || out == nullptr)
+    return TRTV_ERR_INVALID_ARG;
+  if (out_dtype != TRTV_BF16 && out_dtype != TRTV_F32) return TRTV_ERR_INVALID_ARG;
+  if (!aligned(pool, 16) || !aligned(q, 8) || !aligned(out, out_dtype == TRTV_F32 ? 16 : 8))
+    return TRTV_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < pl.ws_total) return TRTV_ERR_WORKSPACE;
+  if (sparse && g->max_pages_per_req > 16384) return TRTV_ERR_UNSUPPORTED;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  AttnParams a{};
+  size_t smem = 0;
+  if (!plan_attn_smem(g, pl, sparse, &a, &smem)) return TRTV_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (!encode_pool_map(g, pl, pool, &map)) return TRTV_ERR_CUDA;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.page_table = pt;
+  a.kv_lens = lens;
+  a.out = out;
+  a.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
+  a.ws_lse = reinterpret_cast<float*>(wsb + pl.ws_lse);
+  a.plan_blocks = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_blocks) : nullptr;
+  a.plan_masks = sparse ? reinterpret_cast<const uint32_t*>(wsb + pl.ws_masks) : nullptr;
+  a.plan_count = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_count) : nullptr;
+  a.err = err;
+  a.batch = g->batch;
+  a.qo_len = g->qo_len;
+  a.num_q_heads = g->num_q_heads;
+  a.num_kv_heads = g->num_kv_heads;
+  a.group = pl.group;
+  a.group_pad = pl.group_pad;
+  a.head_dim = g->head_dim;
+  a.max_pages = g->max_pages_per_req;
+  a.num_slots = g->num_slots;
+  a.slot_stride = g->slot_stride;
+  a.rows = pl.rows;
+  a.rows_pad = pl.rows_pad;
+  a.plan_cap = pl.plan_cap;
+  a.sparse = sparse ? 1 : 0;
+  a.out_f32 = out_dtype == TRTV_F32 ? 1 : 0;
+  a.num_ctas = pl.num_ctas;
+  a.scale_log2 = g->sm_scale * g->k_scale * 1.4426950408889634f;
+  a.v_scale = g->v_scale;
+  cudaError_t e;
+  if (sparse) {
+    e = launch_sparse_plan(block_idx, lens, g->batch, g->qo_len, g->num_kv_heads,
+                           g->max_pages_per_req, topk, pl.plan_cap,
+                           reinterpret_cast<int32_t*>(wsb + pl.ws_blocks),
+                           reinterpret_cast<uint32_t*>(wsb + pl.ws_masks),
+                           reinterpret_cast<int32_t*>(wsb + pl.ws_count), err, st);
+    if (e != cudaSuccess) return TRTV_ERR_CUDA;
+  }
+  e = g->kv_dtype == TRTV_FP8_E4M3
+          ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
+          : launch_attn_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  if (e != cudaSuccess) return TRTV_ERR_CUDA;
+  CombineParams cp{};
+  cp.kv_lens = lens;
+  cp.plan_count = a.plan_count;
+  cp.ws_o = a.ws_o;
+  cp.ws_lse = a.ws_lse;
+  cp.out = out;
+  cp.batch = g->batch;
+  cp.qo_len = g->qo_len;
+  cp.num_q_heads = g->num_q_heads;
+  cp.num_kv_heads = g->num_kv_heads;
+  cp.group = pl.group;
+  cp.group_pad = pl.group_pad;
+  cp.head_dim = g->head_dim;
+  cp.max_pages = g->max_pages_per_req;
+  cp.rows_pad = pl.rows_pad;
+  cp.sparse = a.sparse;
+  cp.out_f32 = a.out_f32;
+  cp.num_ctas = pl.num_ctas;
+  cp.v_scale = g->v_scale;
+  e = launch_combine(cp, pl.n_seq, st);
+  return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
+  const int d = current_device();
+  if (d < 0) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem_set.count({func, d})) return cudaSuccess;
+  }
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, func);
+  if (e != cudaSuccess) return e;
+  if (bytes + fa.sharedSizeBytes > kSmemOptin) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemOptin - fa.sharedSizeBytes));
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_smem_set.insert({func, d});
+  return cudaSuccess;
+}
+
+}  // namespace trtv
+
+using namespace trtv;
+
+extern "C" {
+
+const char* trtv_status_string(trtv_status s) {
+  switch (s) {
+    case TRTV_OK: return "ok";
+    case TRTV_ERR_INVALID_ARG: return "invalid argument";
+    case TRTV_ERR_UNSUPPORTED: return "unsupported geometry";
+    case TRTV_ERR_CUDA: return "CUDA error";
+    case TRTV_ERR_WORKSPACE: return "workspace too small or misaligned";
+  }
+  return "unknown status";
+}
+
+int32_t trtv_version(void) { return 100; }
+
+size_t trtv_workspace_bytes(const trtv_geom* geom, int32_t topk) {
+  Plan pl;
+  if (make_plan(geom, topk, &pl) != TRTV_OK) return 0;
+  return pl.ws_total;
+}
+
+trtv_status trtv_subpage_view(const trtv_geom* g, const int32_t* page_table, const int32_t* kv_lens,
+                              int32_t* k_sub, int32_t* v_sub, void* stream) {
+  if (g == nullptr || page_table == nullptr || kv_lens == nullptr || k_sub == nullptr ||
+      v_sub == nullptr)
+    return TRTV_ERR_INVALID_ARG;
+  if (g->batch < 1 || g->qo_len < 1 || g->max_pages_per_req < 1 || g->num_slots < 1 ||
+      g->slot_stride < 2)
+    return TRTV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(g->num_slots) * g->slot_stride * kGroups + kGroups >= (int64_t{1} << 31))
+    return TRTV_ERR_UNSUPPORTED;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  const cudaError_t e = launch_subpage_view(page_table, kv_lens, k_sub, v_sub, g->batch, g->qo_len,
+                                            g->max_pages_per_req, g->num_slots, g->slot_stride, err,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+
+trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* kv_pool,
+                              const int32_t* page_table, const int32_t* kv_lens, void* out,
+                              int32_t out_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  return attn_common(geom, q, kv_pool, page_table, kv_lens, nullptr, 0, out, out_dtype, workspace,
+                     ws_bytes, stream);
+}
+
+trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                 const int32_t* page_table, const int32_t* kv_lens,
+                                 const int32_t* block_idx, int32_t topk, void* out,
+                                 int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  if (block_idx == nullptr) return TRTV_ERR_INVALID_ARG;
+  return attn_common(geom, q, kv_pool, page_table, kv_lens, block_idx, topk, out, out_dtype,
+                     workspace, ws_bytes, stream);
+}
+
+trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* kv_pool,
+                                 const int32_t* page_table, const int32_t* kv_lens, float* scores,
+                                 void* stream) {
+  Plan pl;
+  trtv_status s = make_plan(g, 0, &pl);
+  if (s != TRTV_OK) return s;
+  if (pl.group > 16) return TRTV_ERR_UNSUPPORTED;
+  if (q == nullptr || kv_pool == nullptr || page_table == nullptr || kv_lens == nullptr ||
+      scores == nullptr)
+    return TRTV_ERR_INVALID_ARG;
+  if (!aligned(kv_pool, 16) || !aligned(q, 8) || !aligned(scores, 4)) return TRTV_ERR_INVALID_ARG;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  ProxyParams a{};
+  size_t smem = 0;
+  if (!plan_proxy_smem(g, pl, &a, &smem)) return TRTV_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (!encode_pool_map(g, pl, kv_pool, &map)) return TRTV_ERR_CUDA;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.page_table = page_table;
+  a.kv_lens = kv_lens;
+  a.scores = scores;
+  a.err = err;
+  a.batch = g->batch;
+  a.qo_len = g->qo_len;
+  a.num_q_heads = g->num_q_heads;
+  a.num_kv_heads = g->num_kv_heads;
+  a.group = pl.group;
+  a.group_pad = pl.group_pad;
+  a.head_dim = g->head_dim;
+  a.max_pages = g->max_pages_per_req;
+  a.num_slots = g->num_slots;
+  a.slot_stride = g->slot_stride;
+  a.rows = pl.rows;
+  a.rows_pad = pl.rows_pad;
+  a.num_ctas = pl.num_ctas;
+  a.score_scale = g->sm_scale * g->k_scale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = g->kv_dtype == TRTV_FP8_E4M3
+                            ? launch_proxy_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
+                            : launch_proxy_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+
+trtv_status trtv_msa_topk(const trtv_geom* g, const float* scores, const int32_t* kv_lens,
+                          int32_t topk, int32_t* block_idx, void* stream) {
+  if (g == nullptr || scores == nullptr || kv_lens == nullptr || block_idx == nullptr)
+    return TRTV_ERR_INVALID_ARG;
+  if (g->batch < 1 || g->qo_len < 1 || g->num_kv_heads < 1 || g->max_pages_per_req < 1)
+    return TRTV_ERR_INVALID_ARG;
+  if (topk < 1 || topk > 1024) return TRTV_ERR_INVALID_ARG;
+  if (g->max_pages_per_req > 16384) return TRTV_ERR_UNSUPPORTED;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  const cudaError_t e = launch_topk(scores, kv_lens, g->batch, g->qo_len, g->num_kv_heads,
+                                    g->max_pages_per_req, topk, block_idx, err,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+
+trtv_status trtv_get_device_error(int32_t* host_out, void* stream) {
+  if (host_out == nullptr) return TRTV_ERR_INVALID_ARG;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return TRTV_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return TRTV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TRTV_ERR_CUDA;
+  *host_out = v;
+  return TRTV_OK;
+}
+
+}  // extern "C"

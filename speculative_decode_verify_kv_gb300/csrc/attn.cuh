@@ -1,0 +1,538 @@
+// attn.cuh -- split-KV ladder verify attention over P128 pages read as
+// grouped-HND [4][kv_head][32][head_dim] sub-pages (dense and MSA sparse).
+//
+// Sources: "Eagle3 for M3 MSA path + CUDA graphs compatibility" (fork PR #3),
+// commit "... verify" (ladder: token t attends kv_len - qo_len + t + 1
+// positions; sparse GQA over selected blocks); "Default Minimax-m3 to unified
+// draft-target kv manager" (#17835), "Grouped-HND draft KV transfer" (page
+// layout); "wrap up eagle changes in m3 side branch" (#18066), view commit
+// (K page at slot * stride, V page at slot * stride + 1).
+//
+// One CTA per SM ("stream-K" split): the work units are the pages (dense) or
+// the unique selected blocks (sparse) of every (request, KV head) sequence,
+// concatenated in sequence order; CTA c takes units [c W / P, (c+1) W / P).
+// A sequence that one CTA covers whole is written as final output; the
+// pieces of a cut sequence are written as (normalised output, log2-sum-exp)
+// partials and merged by combine_kernel.
+//
+// Roles: warp 8 issues TMA tiled loads of each page's K and V sub-pages
+// (128B swizzle) into an NST-stage ring guarded by full/empty mbarriers.
+// Warps 0..7 compute: warp w owns row tile w % MT (16 rows of the
+// (token, group head) tile, row = t * group_pad + g) and the token slice
+// (w / MT) * 16 MT .. + 16 MT of every page.  QK^T and PV run on mma.sync
+// m16n8k16 (bf16, or f16 when the cache is FP8), fp32 accumulation, online
+// softmax in the log2 domain.  At the end of a sequence the 8 / MT slice
+// partials of each row tile are merged in fixed order through shared memory.
+#pragma once
+
+#include "common.cuh"
+
+namespace trtv {
+
+template <int D>
+struct Shape {
+  static constexpr int KS = D / 16;  // k-steps of QK^T
+  static constexpr int DT = D / 8;   // n-tiles (8 columns) of PV
+};
+
+// Loads the A fragments of Q for one 16-row tile.  Rows beyond the
+// (qo_len x group) tile are zero.  FP8 caches use f16 operands and a
+// permuted k order (k-step ks, lane quad c: head dims 32c + 4ks + {0..3}).
+template <bool FP8, int D>
+__device__ __forceinline__ void load_q_frags(const __nv_bfloat16* q, int T, int Hq, int G, int Gp,
+                                             int b, int h, int mt, uint32_t (&qa)[D / 16][4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const __nv_bfloat16* rowp[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int r = mt * 16 + g + 8 * hh;
+    const int t = r / Gp, gl = r % Gp;
+    rowp[hh] = (t < T && gl < G)
+                   ? q + ((static_cast<int64_t>(b) * T + t) * Hq + static_cast<int64_t>(h) * G + gl) * D
+                   : nullptr;
+  }
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t lo = 0, hi = 0;
+      if (rowp[hh] != nullptr) {
+        if constexpr (FP8) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(rowp[hh] + 32 * c + 4 * ks));
+          lo = bf16x2_to_f16x2(v.x);
+          hi = bf16x2_to_f16x2(v.y);
+        } else {
+          lo = __ldg(reinterpret_cast<const uint32_t*>(rowp[hh] + 16 * ks + 2 * c));
+          hi = __ldg(reinterpret_cast<const uint32_t*>(rowp[hh] + 16 * ks + 8 + 2 * c));
+        }
+      }
+      qa[ks][hh] = lo;       // a0 (row g) / a1 (row g+8): k = 2c, 2c+1
+      qa[ks][2 + hh] = hi;   // a2 / a3: k = 2c+8, 2c+9
+    }
+  }
+}
+
+// Sequence cursor over the CTA's unit range.  Dense: items are requests
+// (every KV head of a request has the same page count); sparse: items are
+// (request, KV head) sequences.
+struct SeqCursor {
+  int b, h, s;
+  int64_t start, units;
+};
+
+__device__ __forceinline__ int64_t item_start(const int32_t* scan, int i, int Hk, bool sparse) {
+  return sparse ? static_cast<int64_t>(scan[i]) : static_cast<int64_t>(scan[i]) * Hk;
+}
+
+__device__ __forceinline__ void cursor_fill(SeqCursor& cur, const int32_t* scan, int Hk,
+                                            bool sparse) {
+  if (sparse) {
+    cur.start = scan[cur.s];
+    cur.units = scan[cur.s + 1] - scan[cur.s];
+  } else {
+    const int64_t u = scan[cur.b + 1] - scan[cur.b];
+    cur.start = static_cast<int64_t>(scan[cur.b]) * Hk + cur.h * u;
+    cur.units = u;
+  }
+}
+
+// First sequence holding unit u0 (u0 < W).
+__device__ __forceinline__ SeqCursor cursor_first(const int32_t* scan, int n, int Hk, bool sparse,
+                                                  int64_t u0) {
+  int lo = 0, hi = n;  // last item i with start(i) <= u0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (item_start(scan, mid, Hk, sparse) <= u0) lo = mid; else hi = mid - 1;
+  }
+  SeqCursor cur;
+  if (sparse) {
+    cur.s = lo; cur.b = lo / Hk; cur.h = lo % Hk;
+  } else {
+    const int64_t u = scan[lo + 1] - scan[lo];
+    cur.b = lo;
+    cur.h = static_cast<int>((u0 - static_cast<int64_t>(scan[lo]) * Hk) / u);
+    cur.s = lo * Hk + cur.h;
+  }
+  cursor_fill(cur, scan, Hk, sparse);
+  return cur;
+}
+
+__device__ __forceinline__ void cursor_next(SeqCursor& cur, const int32_t* scan, int n, int Hk,
+                                            bool sparse) {
+  if (sparse) {
+    do { ++cur.s; } while (cur.s < n && scan[cur.s + 1] == scan[cur.s]);
+    cur.b = cur.s / Hk; cur.h = cur.s % Hk;
+  } else {
+    if (++cur.h == Hk) {
+      cur.h = 0;
+      do { ++cur.b; } while (cur.b < n && scan[cur.b + 1] == scan[cur.b]);
+    }
+    cur.s = cur.b * Hk + cur.h;
+  }
+  if ((sparse ? cur.s : cur.b) < n) cursor_fill(cur, scan, Hk, sparse);
+}
+
+template <bool FP8, int D, int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ AttnParams p) {
+  constexpr bool F16 = FP8;                      // mma operand type for FP8 caches
+  constexpr int NB = FP8 ? 1 : (D * 2) / 128;    // TMA boxes per cache token row
+  constexpr int SUBK = NB * kBox;                // bytes of one K (or V) sub-page in a stage
+  constexpr int SUBV = FP8 ? 2 * kBox : SUBK;    // bytes of one V sub-page as PV reads it
+  constexpr int TS = 16 * MT;                    // tokens of a page per warp
+  constexpr int CH = TS < 32 ? TS : 32;          // tokens per score chunk
+  constexpr int NCH = TS / CH;
+  constexpr int NT = CH / 8;
+  constexpr int KS = Shape<D>::KS;
+  constexpr int DT = Shape<D>::DT;
+  constexpr int NSL = kConsumerWarps / MT;       // token slices per page
+  constexpr int HALF = D / 2 < 64 ? D / 2 : 64;  // merge columns per pass
+  constexpr int MSTR = HALF + 8;                 // merge row stride (floats)
+  static_assert(!FP8 || D == 128, "FP8 caches need head_dim 128");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  uint64_t* empty = full + p.nstages;
+  int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
+  const bool sparse = p.sparse != 0;
+  const int Hk = p.num_kv_heads, T = p.qo_len, NST = p.nstages;
+  const int nitems = sparse ? p.batch * Hk : p.batch;
+  int32_t* warp_tot = scan + nitems + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  block_exclusive_scan(nitems, scan, warp_tot, [&](int i) -> int32_t {
+    if (sparse) return p.plan_count[i];
+    const int L = p.kv_lens[i];
+    if (len_valid(L, T, p.max_pages)) return (L + kPage - 1) / kPage;
+    if (blockIdx.x == 0) atomicOr(p.err, TRTV_DEVERR_KV_LEN);
+    return 0;
+  });
+  const int64_t W = item_start(scan, nitems, Hk, sparse);
+  if (W == 0) return;
+  const int64_t u0 = cta_unit_begin(blockIdx.x, W, p.num_ctas);
+  const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);
+  if (u0 >= u1) return;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    prefetch_tensormap(&kv_map);
+    const uint64_t pol = policy_evict_first();
+    const int sub_rows = Hk * kSub;  // tensor-map rows per sub-page buffer group
+    int it = 0;
+    bool alive = true;
+    for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+         alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+         cursor_next(cur, scan, nitems, Hk, sparse)) {
+      const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
+      const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+      for (int64_t j = j0; j < j1; ++j, ++it) {
+        const int st = it % NST;
+        const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
+        if (it >= NST && !mbar_wait(&empty[st], ph ^ 1u, p.err)) { alive = false; break; }
+        const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
+                               : static_cast<int>(j);
+        int slot = p.page_table[static_cast<int64_t>(cur.b) * p.max_pages + blk];
+        if (slot < 0 || slot >= p.num_slots) {
+          atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
+          slot = 0;
+        }
+        uint8_t* stage = smem + p.off_stage + st * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(p.stage_bytes));
+        const int64_t kbuf = static_cast<int64_t>(slot) * p.slot_stride;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          uint8_t* dst = stage + (kv ? p.off_v : p.off_k);
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+            const int y = static_cast<int>(((kbuf + kv) * kGroups + g) * sub_rows + cur.h * kSub);
+#pragma unroll
+            for (int hb = 0; hb < NB; ++hb)
+              tma_load_2d(dst + (g * NB + hb) * kBox, &kv_map, &full[st], hb * (FP8 ? 128 : 64), y,
+                          pol);
+          }
+        }
+      }
+    }
+    // never leave copies in flight: wait for the last issued pages to land
+    for (int k = (it > NST ? it - NST : 0); k < it; ++k)
+      mbar_wait(&full[k % NST], static_cast<uint32_t>(k / NST) & 1u, p.err);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, c = lane & 3;
+  const int mt = warp % MT, sl = warp / MT;
+  const int tok0 = sl * TS;
+  float* mbuf = reinterpret_cast<float*>(smem + p.off_merge);
+  float* ml = reinterpret_cast<float*>(smem + p.off_ml);          // [8 warps][16 rows][2]
+  float* mlf = ml + kConsumerWarps * 32;                          // [128 rows][2] final
+  bool dead = false;
+  int it = 0;
+
+  for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+       (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+       cursor_next(cur, scan, nitems, Hk, sparse)) {
+    const int b = cur.b, h = cur.h;
+    const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
+    const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+    const int L = p.kv_lens[b];
+
+    uint32_t qa[KS][4];
+    load_q_frags<FP8, D>(p.q, T, p.num_q_heads, p.group, p.group_pad, b, h, mt, qa);
+    int bound[2], trow[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = mt * 16 + g + 8 * hh;
+      const int t = r / p.group_pad, gl = r % p.group_pad;
+      const bool ok = t < T && gl < p.group;
+      trow[hh] = ok ? t : 0;
+      bound[hh] = ok ? L - T + t : -1;
+    }
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    float o[DT][4];
+#pragma unroll
+    for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    for (int64_t j = j0; j < j1; ++j, ++it) {
+      const int st = it % NST;
+      const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
+      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, p.err));
+      int blk = static_cast<int>(j);
+      uint32_t tokmask = 0xffffffffu;
+      if (sparse) {
+        blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+        tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+      }
+      const int pos0 = blk * kPage;
+      int bnd[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) bnd[hh] = ((tokmask >> trow[hh]) & 1u) ? bound[hh] : -1;
+      const uint8_t* stage = smem + p.off_stage + st * p.stage_bytes;
+      const uint8_t* kst = stage + p.off_k;
+      const uint8_t* vst;
+      if constexpr (FP8) {
+        // convert this warp's 16 rows of V to f16 (zero past kv_len), shared by the slice
+        uint8_t* conv = smem + p.off_conv + (it & 1) * (kGroups * 2 * kBox);
+        const int trow0 = tok0 + mt * 16;
+        const int sp = trow0 / kSub, r00 = trow0 % kSub;
+        const uint8_t* vsrc = stage + p.off_v + sp * kBox;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int i = lane + 32 * q4;
+          const int r = r00 + (i >> 3), ch = i & 7;
+          uint4 raw = *reinterpret_cast<const uint4*>(vsrc + sw128(r, ch));
+          if (pos0 + sp * kSub + r >= L) raw = make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t f[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            f[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
+            f[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
+          }
+          uint8_t* dst = conv + sp * 2 * kBox + (ch >> 2) * kBox;
+          const int cb = 2 * (ch & 3);
+          *reinterpret_cast<uint4*>(dst + sw128(r, cb)) = make_uint4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<uint4*>(dst + sw128(r, cb + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+        }
+        if (MT == 1) __syncwarp(); else named_barrier(2 + sl, MT * 32);
+        vst = conv;
+      } else {
+        vst = stage + p.off_v;
+      }
+
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int ct = tok0 + cc * CH;          // chunk start within the page
+        const int sp = ct / kSub, r0 = ct % kSub;
+        float s[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+        // ---- S = Q K^T over the chunk
+        if constexpr (FP8) {
+          const uint8_t* kb = kst + sp * kBox;
+#pragma unroll
+          for (int jt = 0; jt < NT; ++jt) {
+            const int r = r0 + 8 * jt + g;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(kb + sw128(r, 2 * c));
+            const uint4 w1 = *reinterpret_cast<const uint4*>(kb + sw128(r, 2 * c + 1));
+            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[ks] & 0xffffu));
+              const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[ks] >> 16));
+              mma16816<F16>(s[jt], qa[ks], b0, b1);
+            }
+          }
+        } else {
+          const uint8_t* kb = kst + sp * SUBK;
+          const int mat = lane >> 3, rr = lane & 7;
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const int dch = 2 * ks + (mat & 1);
+#pragma unroll
+            for (int jp = 0; jp < NT / 2; ++jp) {
+              const int r = r0 + 8 * (2 * jp + (mat >> 1)) + rr;
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(smem_u32(kb + (dch >> 3) * kBox + sw128(r, dch & 7)), b0, b1, b2, b3);
+              mma16816<F16>(s[2 * jp], qa[ks], b0, b1);
+              mma16816<F16>(s[2 * jp + 1], qa[ks], b2, b3);
+            }
+          }
+        }
+        // ---- mask (ladder bound, selected tokens, kv_len) and online softmax
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int jt = 0; jt < NT; ++jt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pos = pos0 + ct + 8 * jt + 2 * c + (e & 1);
+            const float x = s[jt][e] * p.scale_log2;
+            s[jt][e] = (pos <= bnd[e >> 1]) ? x : -INFINITY;
+            mx[e >> 1] = fmaxf(mx[e >> 1], s[jt][e]);
+          }
+        }
+        float alpha[2], muse[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
+          mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
+          const float mn = fmaxf(m_r[hh], mx[hh]);
+          muse[hh] = (mn == -INFINITY) ? 0.f : mn;
+          alpha[hh] = fast_exp2(m_r[hh] - muse[hh]);
+          m_r[hh] = mn;
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int jt = 0; jt < NT; ++jt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            s[jt][e] = fast_exp2(s[jt][e] - muse[e >> 1]);
+            rs[e >> 1] += s[jt][e];
+          }
+        }
+        l_r[0] = l_r[0] * alpha[0] + rs[0];
+        l_r[1] = l_r[1] * alpha[1] + rs[1];
+#pragma unroll
+        for (int i = 0; i < DT; ++i) {
+          o[i][0] *= alpha[0]; o[i][1] *= alpha[0];
+          o[i][2] *= alpha[1]; o[i][3] *= alpha[1];
+        }
+        // ---- O += P V
+        const uint8_t* vb = vst + sp * SUBV;
+        const bool tail = pos0 + ct + CH > L;   // rows past kv_len may hold anything
+        const int mat = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk) {
+          uint32_t a[4];
+          a[0] = pack2<F16>(s[2 * kk][0], s[2 * kk][1]);
+          a[1] = pack2<F16>(s[2 * kk][2], s[2 * kk][3]);
+          a[2] = pack2<F16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+          a[3] = pack2<F16>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+          uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+          if (!FP8 && tail) {
+            const int pb = pos0 + ct + 16 * kk + 2 * c;
+            mlo = (pb < L ? 0x0000ffffu : 0u) | (pb + 1 < L ? 0xffff0000u : 0u);
+            mhi = (pb + 8 < L ? 0x0000ffffu : 0u) | (pb + 9 < L ? 0xffff0000u : 0u);
+          }
+          const int r = r0 + 16 * kk + 8 * (mat & 1) + rr;
+#pragma unroll
+          for (int dp = 0; dp < DT / 2; ++dp) {
+            const int dch = 2 * dp + (mat >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(smem_u32(vb + (dch >> 3) * kBox + sw128(r, dch & 7)), b0, b1, b2, b3);
+            mma16816<F16>(o[2 * dp], a, b0 & mlo, b1 & mhi);
+            mma16816<F16>(o[2 * dp + 1], a, b2 & mlo, b3 & mhi);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // ---------------------------------------------------------- sequence end
+    l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 1);
+    l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 2);
+    l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 1);
+    l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 2);
+    const bool whole = u0 <= cur.start && cur.start + cur.units <= u1;
+    const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (cur.start <= u0 ? 0 : 1);
+    const int64_t obase = static_cast<int64_t>(b) * T;
+
+    if constexpr (NSL == 1) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = mt * 16 + g + 8 * hh;
+        const int t = r / p.group_pad, gl = r % p.group_pad;
+        if (t >= T || gl >= p.group) continue;
+        const float inv = l_r[hh] > 0.f ? 1.f / l_r[hh] : 0.f;
+        const float sc = whole ? inv * p.v_scale : inv;
+        if (whole) {
+          const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(h) * p.group + gl) * D;
+#pragma unroll
+          for (int i = 0; i < DT; ++i) {
+            const float v0 = o[i][2 * hh] * sc, v1 = o[i][2 * hh + 1] * sc;
+            if (p.out_f32)
+              *reinterpret_cast<float2*>(static_cast<float*>(p.out) + orow + 8 * i + 2 * c) = make_float2(v0, v1);
+            else
+              *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + orow + 8 * i + 2 * c) =
+                  __floats2bfloat162_rn(v0, v1);
+          }
+        } else {
+          float* dst = p.ws_o + (slot * p.rows_pad + r) * D;
+#pragma unroll
+          for (int i = 0; i < DT; ++i)
+            *reinterpret_cast<float2*>(dst + 8 * i + 2 * c) = make_float2(o[i][2 * hh] * sc, o[i][2 * hh + 1] * sc);
+          if (c == 0)
+            p.ws_lse[slot * p.rows_pad + r] = l_r[hh] > 0.f ? m_r[hh] + __log2f(l_r[hh]) : -INFINITY;
+        }
+      }
+    } else {
+      if (c == 0) {
+        ml[(warp * 16 + g) * 2 + 0] = m_r[0];
+        ml[(warp * 16 + g) * 2 + 1] = l_r[0];
+        ml[(warp * 16 + g + 8) * 2 + 0] = m_r[1];
+        ml[(warp * 16 + g + 8) * 2 + 1] = l_r[1];
+      }
+      named_barrier(1, kConsumerWarps * 32);
+      float f[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int rl = g + 8 * hh;
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < NSL; ++q) M = fmaxf(M, ml[((q * MT + mt) * 16 + rl) * 2]);
+        const float Mu = (M == -INFINITY) ? 0.f : M;
+        float Ls = 0.f;
+#pragma unroll
+        for (int q = 0; q < NSL; ++q)
+          Ls += ml[((q * MT + mt) * 16 + rl) * 2 + 1] * fast_exp2(ml[((q * MT + mt) * 16 + rl) * 2] - Mu);
+        f[hh] = Ls > 0.f ? fast_exp2(m_r[hh] - Mu) / Ls : 0.f;
+        if (sl == 0 && c == 0) {
+          mlf[(mt * 16 + rl) * 2 + 0] = Mu;
+          mlf[(mt * 16 + rl) * 2 + 1] = Ls;
+        }
+      }
+#pragma unroll
+      for (int half = 0; half < D / HALF; ++half) {
+        for (int q = 0; q < NSL; ++q) {
+          if (sl == q) {
+#pragma unroll
+            for (int i = 0; i < HALF / 8; ++i) {
+              const int di = half * (HALF / 8) + i;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                float2* dst = reinterpret_cast<float2*>(mbuf + (mt * 16 + g + 8 * hh) * MSTR + 8 * i + 2 * c);
+                float2 v = make_float2(o[di][2 * hh] * f[hh], o[di][2 * hh + 1] * f[hh]);
+                if (q != 0) { const float2 u = *dst; v.x += u.x; v.y += u.y; }
+                *dst = v;
+              }
+            }
+          }
+          named_barrier(1, kConsumerWarps * 32);
+        }
+        // cooperative write-out of this column half (4 columns per item)
+        const int tid = threadIdx.x;
+        const int items = MT * 16 * (HALF / 4);
+        for (int idx = tid; idx < items; idx += kConsumerWarps * 32) {
+          const int r = idx / (HALF / 4), c4 = idx % (HALF / 4);
+          const int t = r / p.group_pad, gl = r % p.group_pad;
+          if (t >= T || gl >= p.group) continue;
+          float4 v = *reinterpret_cast<const float4*>(mbuf + r * MSTR + 4 * c4);
+          const int d = half * HALF + 4 * c4;
+          if (whole) {
+            v.x *= p.v_scale; v.y *= p.v_scale; v.z *= p.v_scale; v.w *= p.v_scale;
+            const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(h) * p.group + gl) * D;
+            if (p.out_f32) {
+              *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + d) = v;
+            } else {
+              __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+              uint2 pk;
+              pk.x = *reinterpret_cast<uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow + d) = pk;
+            }
+          } else {
+            *reinterpret_cast<float4*>(p.ws_o + (slot * p.rows_pad + r) * D + d) = v;
+            if (half == 0 && c4 == 0) {
+              const float Mu = mlf[r * 2], Ls = mlf[r * 2 + 1];
+              p.ws_lse[slot * p.rows_pad + r] = Ls > 0.f ? Mu + __log2f(Ls) : -INFINITY;
+            }
+          }
+        }
+        named_barrier(1, kConsumerWarps * 32);
+      }
+    }
+  }
+}
+
+}  // namespace trtv

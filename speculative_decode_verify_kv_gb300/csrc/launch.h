@@ -1,0 +1,39 @@
+// launch.h -- host-side launchers of the kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace trtv {
+
+struct AttnParams;
+struct ProxyParams;
+struct CombineParams;
+
+// attention: head_dim in {64, 128}; mt (row tiles of 16) in {1, 2, 4, 8}
+cudaError_t launch_attn_bf16(int head_dim, int mt, const CUtensorMap& map, const AttnParams& p,
+                             int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_attn_fp8(int head_dim, int mt, const CUtensorMap& map, const AttnParams& p,
+                            int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_proxy_bf16(int head_dim, int mt, const CUtensorMap& map, const ProxyParams& p,
+                              int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_proxy_fp8(int head_dim, int mt, const CUtensorMap& map, const ProxyParams& p,
+                             int grid, size_t smem, cudaStream_t st);
+
+cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t* k_sub,
+                                int32_t* v_sub, int batch, int qo_len, int max_pages,
+                                int num_slots, int stride, int* err, cudaStream_t st);
+cudaError_t launch_combine(const CombineParams& p, int n_seq, cudaStream_t st);
+cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
+                               int num_kv_heads, int max_pages, int topk, int plan_cap,
+                               int32_t* plan_blocks, uint32_t* plan_masks, int32_t* plan_count,
+                               int* err, cudaStream_t st);
+cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int qo_len,
+                        int num_kv_heads, int max_pages, int topk, int32_t* out, int* err,
+                        cudaStream_t st);
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+cudaError_t ensure_smem_attr(const void* func, size_t bytes);
+
+}  // namespace trtv
