@@ -1,0 +1,488 @@
+"""Benchmark: multi-token speculative-decoding verify attention on one GB300.
+
+Headline workload ("dense"): batch 64, qo_len 4, kv_len ~ U{1024..8192},
+32 query / 4 KV heads, head_dim 128, bf16 K/V in P128 pages read through the
+P32 grouped-HND view, bf16 output.  One step = one verify pass of that batch:
+the P32 sub-page view (trtv_subpage_view) and the dense ladder attention with
+its split-KV combine (trtv_verify_dense).  The MSA sparse pass (proxy scores
+-> per-token top-k -> sparse attention) is timed the same way on the "msa"
+workload (batch 32, kv_len ~ U{16384..65536}, 64 / 4 heads, top-k 16) and
+reported under "paths".
+
+value      query tokens per second (batch * qo_len per step), whole job
+e2e        the same through the C ABI with per-step host->device copies of
+           q / page table / kv_lens from pinned memory and the output read back
+roofline   the dominant call (trtv_verify_dense: attention + combine) against
+           the measured HBM copy bandwidth; algorithmic bytes = K and V of
+           every visible position + Q + O
+cpu_baseline  the fp64 oracle on a bounded sample of the same workload
+
+--impl reference runs the fp64 oracle as the reference arm (there is no
+runnable reference implementation; see the design notes).
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify query-tokens/s and KV HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "query-tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 7900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decode_verify_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current kernel
+    sources (profiles/dram_traffic.txt), else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        m = re.match(r"^(\S+)\s+(\S+)\s+([0-9a-f]+)\s+(\d+)", line)
+        if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == want:
+            return int(m.group(4))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while running."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1 + 0.15]
+        note = None
+        if not inside:
+            inside = [r for (t, r) in self.rows]
+            note = "timed region shorter than the 100 ms sampling period; samples around it"
+        mhz, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                maxs.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        out = {"sm_mhz": float(np.median(mhz)) if mhz else None,
+               "sm_max_mhz": float(max(maxs)) if maxs else None,
+               "reasons": sorted(reasons), "samples": len(mhz)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+
+def dense_bytes(p) -> int:
+    elem = p.kv_elem_bytes()
+    kv = int(p.kv_lens.sum())
+    kv_bytes = kv * p.num_kv_heads * p.head_dim * elem * 2
+    q_bytes = p.q.numel() * 2
+    o_bytes = p.q.numel() * (4 if p.out_dtype == "f32" else 2)
+    return kv_bytes + q_bytes + o_bytes
+
+
+def proxy_bytes(p) -> int:
+    elem = p.kv_elem_bytes()
+    k_bytes = int(p.kv_lens.sum()) * p.num_kv_heads * p.head_dim * elem
+    return k_bytes + p.q.numel() * 2 + p.batch * p.qo_len * p.num_kv_heads * p.max_pages_per_req * 4
+
+
+def sparse_bytes(p, idx: np.ndarray):
+    """K and V of the visible positions of each unique selected block, per
+    (request, KV head), + Q + O + indices.  Also returns the mean unique count."""
+    elem = p.kv_elem_bytes()
+    lens = p.kv_lens.numpy()
+    pos = 0
+    uniq = []
+    for b in range(p.batch):
+        L = int(lens[b])
+        npg = (L + 127) // 128
+        for h in range(p.num_kv_heads):
+            u = np.unique(idx[b, :, h, :])
+            u = u[(u >= 0) & (u < npg)]
+            uniq.append(len(u))
+            pos += int(np.minimum(128, L - 128 * u).sum())
+    kv = pos * p.head_dim * elem * 2
+    return kv + p.q.numel() * 2 + p.q.numel() * 2 + idx.size * 4, float(np.mean(uniq))
+
+
+# ---------------------------------------------------------------------------
+
+_CACHE = {}
+BATCH = None   # --batch: first requests only (profiling captures), else the full batch
+
+
+def make(name):
+    from speculative_decode_verify_kv_gb300 import workloads as W
+    if name not in _CACHE:
+        _CACHE[name] = W.make_workload(name, batch=BATCH)
+    return _CACHE[name]
+
+
+def describe(p, name):
+    return {"workload": f"{name}: batch {p.batch}, qo_len {p.qo_len}, {p.num_q_heads}/{p.num_kv_heads} "
+                        f"heads, head_dim {p.head_dim}, {p.kv_dtype} K/V, P128 pages via P32 "
+                        f"grouped-HND view, stride {p.slot_stride}" + (f", top-k {p.topk}" if p.topk else ""),
+            "batch": p.batch, "qo_len": p.qo_len, "num_q_heads": p.num_q_heads,
+            "num_kv_heads": p.num_kv_heads, "head_dim": p.head_dim, "kv_dtype": p.kv_dtype,
+            "kv_len_mean": float(p.kv_lens.float().mean()), "kv_len_total": int(p.kv_lens.sum()),
+            "pool_slots": p.num_slots, "max_pages_per_req": p.max_pages_per_req,
+            "seed": 1000 + ["tiny", "dense", "msa", "fp8", "long"].index(name)}
+
+
+def time_path(name, steps, warmup, sampler=None):
+    """Device-time `steps` verify passes of workload `name` (inputs resident in HBM)."""
+    import torch
+    from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
+    p = make(name)
+    dv = DeviceVerify(p)
+    msa = p.topk > 0
+    if msa:
+        calls = [("proxy", dv.proxy), ("topk", dv.select), ("sparse", dv.sparse)]
+        launches = 5   # proxy, topk, plan, attention, combine
+    else:
+        calls = [("subpage_view", dv.subpage_view), ("verify_dense", dv.dense)]
+        launches = 3   # sub-page view, attention, combine
+    for _ in range(warmup):
+        for _, f in calls:
+            f()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record()
+    for k in range(steps):
+        e = ev[k]
+        e[0].record()
+        for i, (_, f) in enumerate(calls):
+            f()
+            e[i + 1].record()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    total_ms = start.elapsed_time(end)
+    per_call = {}
+    for i, (n, _) in enumerate(calls):
+        per_call[n] = float(np.mean([ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps)]))
+    from speculative_decode_verify_kv_gb300 import trtv_get_device_error
+    derr = trtv_get_device_error()
+    res = {"p": p, "dv": dv, "ms_per_step": total_ms / steps, "per_call_ms": per_call,
+           "t0": t0, "t1": t1, "launches_per_step": launches, "device_error": derr}
+    if msa:
+        idx = dv.block_idx.cpu().numpy()
+        sb, umean = sparse_bytes(p, idx)
+        res["bytes"] = {"proxy": proxy_bytes(p), "sparse": sb, "topk": p.batch * p.qo_len * p.num_kv_heads * (p.max_pages_per_req * 4 + p.topk * 4)}
+        res["unique_blocks_mean"] = umean
+    else:
+        res["bytes"] = {"verify_dense": dense_bytes(p),
+                        "subpage_view": p.batch * p.max_pages_per_req * (4 + 32) + p.batch * 4}
+    return res
+
+
+def time_e2e(name, steps, warmup):
+    """Same step through the C ABI with host buffers: per step, H2D of q,
+    page table and kv_lens from pinned memory, the kernels, D2H of the output."""
+    import torch
+    from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
+    p = make(name)
+    dv = DeviceVerify(p)
+    hq = p.q.pin_memory()
+    hpt = p.page_table.pin_memory()
+    hl = p.kv_lens.pin_memory()
+    hout = torch.empty(dv.out.shape, dtype=dv.out.dtype).pin_memory()
+    msa = p.topk > 0
+
+    def step():
+        dv.q.copy_(hq, non_blocking=True)
+        dv.page_table.copy_(hpt, non_blocking=True)
+        dv.kv_lens.copy_(hl, non_blocking=True)
+        if msa:
+            dv.msa()
+        else:
+            dv.subpage_view()
+            dv.dense()
+        hout.copy_(dv.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = hq.numel() * hq.element_size() + hpt.numel() * 4 + hl.numel() * 4
+    d2h = hout.numel() * hout.element_size()
+    return {"value": p.batch * p.qo_len / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def cpu_baseline(name, budget_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload's
+    requests (same pool); throughput scaled to query tokens/s."""
+    import oracle
+    p = make(name)
+    Tq = p.qo_len
+    import torch
+    n = 1
+    spent = 0.0
+    while True:
+        reqs = list(range(min(n, p.batch)))
+        rows = torch.cat([torch.arange(b * Tq, (b + 1) * Tq) for b in reqs])
+        x = oracle.Inputs(p, q=p.q[rows], page_table=p.page_table[reqs].contiguous(),
+                          kv_lens=p.kv_lens[reqs].contiguous(), batch=len(reqs))
+        t0 = time.perf_counter()
+        if p.topk:
+            s, _ = oracle.proxy_score(x)
+            idx, _ = oracle.topk(x, s, p.topk)
+            oracle.sparse_attn(x, idx)
+        else:
+            oracle.subpage_view(x)
+            oracle.verify_dense(x)
+        dt = time.perf_counter() - t0
+        spent += dt
+        if dt > budget_s / 4 or len(reqs) == p.batch or spent > budget_s:
+            break
+        n *= 2
+    return {"value": len(reqs) * Tq / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {len(reqs)} of {p.batch} requests of the {name} workload "
+                      f"({int(p.kv_lens[:len(reqs)].sum())} KV positions), one pass, {dt:.2f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle on the host cores, each step a bounded
+    sample (4 requests, rotating) of the same workload."""
+    import torch
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    p = make(args.workload)
+    Tq = p.qo_len
+    per = min(4, p.batch)
+
+    def step(k):
+        reqs = [(k * per + i) % p.batch for i in range(per)]
+        rows = torch.cat([torch.arange(b * Tq, (b + 1) * Tq) for b in reqs])
+        x = oracle.Inputs(p, q=p.q[rows], page_table=p.page_table[reqs].contiguous(),
+                          kv_lens=p.kv_lens[reqs].contiguous(), batch=len(reqs))
+        if p.topk:
+            s, _ = oracle.proxy_score(x)
+            idx, _ = oracle.topk(x, s, p.topk)
+            oracle.sparse_attn(x, idx)
+        else:
+            oracle.subpage_view(x)
+            oracle.verify_dense(x)
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(args.warmup + k)
+    dt = time.perf_counter() - t0
+    value = per * Tq * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": describe(p, args.workload),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{per} requests per step of the {args.workload} workload"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="dense", choices=["dense", "msa", "fp8", "long"])
+    ap.add_argument("--paths", default="msa", help="extra workloads timed alongside (comma list)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep only the first requests of each workload (small profiling case)")
+    args = ap.parse_args()
+    global BATCH
+    BATCH = args.batch
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import speculative_decode_verify_kv_gb300 as T
+    from speculative_decode_verify_kv_gb300 import _build
+    _build.build()
+    T.load()
+    T.trtv_get_device_error()
+
+    sampler = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    head = time_path(args.workload, args.steps, args.warmup, sampler)
+    sampler.stop()
+    clocks = sampler.summary(head["t0"], head["t1"])
+    ms = head["ms_per_step"]
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    p = head["p"]
+    qtok = p.batch * p.qo_len
+    value = qtok * world / (ms / 1e3)
+
+    peak, peak_kind = peaks()
+    dom = "proxy" if p.topk else "verify_dense"
+    dom_ms = head["per_call_ms"][dom]
+    dom_bytes = head["bytes"][dom]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    step_bytes = sum(head["bytes"].values())
+    kernel_name = "proxy_kernel" if p.topk else "attn_kernel+combine_kernel"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": ncu_traffic(dom, args.workload),
+                "kernel": f"{dom} ({kernel_name})", "peak_kind": f"of {peak_kind}",
+                "algorithmic_bytes": dom_bytes, "launch_ms": dom_ms,
+                "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS}
+
+    paths = {}
+    for extra in [w for w in args.paths.split(",") if w and w not in (args.workload, "none")]:
+        r = time_path(extra, max(10, args.steps // 4), args.warmup)
+        pe = r["p"]
+        per = {}
+        for n, b in r["bytes"].items():
+            per[n] = {"ms": r["per_call_ms"][n], "bytes": b,
+                      "gbs": b / (r["per_call_ms"][n] / 1e3) / 1e9,
+                      "frac": b / (r["per_call_ms"][n] / 1e3) / 1e9 / peak}
+        pv = {"config": describe(pe, extra), "ms_per_step": r["ms_per_step"],
+              "value": pe.batch * pe.qo_len / (r["ms_per_step"] / 1e3), "unit": UNIT,
+              "step_gbs": sum(r["bytes"].values()) / (r["ms_per_step"] / 1e3) / 1e9,
+              "calls": per, "device_error": r["device_error"],
+              "gpu_launches_per_step": r["launches_per_step"]}
+        if "unique_blocks_mean" in r:
+            pv["unique_blocks_mean"] = r["unique_blocks_mean"]
+        paths[extra] = pv
+        del r
+        torch.cuda.empty_cache()
+
+    e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)
+    if dist and e2e:
+        t = torch.tensor([e2e["ms_per_step"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["value"] = qtok * world / (float(t.item()) / 1e3)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": p.kv_dtype.replace("fp8_e4m3", "fp8e4m3"),
+            "data": "synthetic",
+            "config": dict(describe(p, args.workload),
+                           l2=f"inputs larger than L2: {dom_bytes / 2**20:.0f} MiB of KV read per "
+                              f"step vs {L2_BYTES / 2**20:.0f} MiB L2, no flush",
+                           parallelism="replicas" if world > 1 else "single GPU"),
+            "kv_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,
+            "kv_hbm_pct_of_measured_peak": 100 * step_bytes / (ms / 1e3) / 1e9 / peak,
+            "per_call_ms": head["per_call_ms"], "roofline": roofline,
+            "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+                    if e2e else None),
+            "gpu_launches": head["launches_per_step"] * args.steps, "clocks": clocks,
+            "device_error": head["device_error"], "paths": paths}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

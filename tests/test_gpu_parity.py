@@ -95,7 +95,9 @@ def test_dense_split_invariance(num_ctas):
     dv2 = DeviceVerify(p, num_ctas=1, out_dtype="f32")
     o2 = dv2.dense()
     torch.cuda.synchronize()
-    assert (dv1.out - o2).abs().max().item() < 1e-4
+    # a split changes the running maximum that P is rounded against before the
+    # bf16 PV product, so splits agree to bf16 rounding of P, not fp32 rounding
+    assert (dv1.out - o2).abs().max().item() < 5e-3
 
 
 @pytest.mark.parametrize("Hq,Hk,Tq,D", [
@@ -318,7 +320,7 @@ def test_sparse_full_k_equals_dense():
     dv.select()
     sp = dv.sparse()
     torch.cuda.synchronize()
-    assert (dense - sp).abs().max().item() < 1e-4
+    assert (dense - sp).abs().max().item() < 5e-3
 
 
 def test_sparse_handmade_indices():
