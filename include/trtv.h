@@ -93,9 +93,10 @@ typedef struct {
   float sm_scale;            /* softmax scale, e.g. 1 / sqrt(D) */
   float k_scale;             /* per-tensor dequantisation scale of K (1 for bf16) */
   float v_scale;             /* per-tensor dequantisation scale of V (1 for bf16) */
-  int32_t num_ctas;          /* work CTAs of the attention / proxy kernels;
-                                0 = one per SM (results do not depend on it
-                                beyond fp32 rounding) */
+  int32_t num_ctas;          /* work CTAs of the attention / proxy kernels,
+                                0..1024; 0 = one per SM.  Results depend on it
+                                only through rounding (a split changes the
+                                running maximum P is rounded against). */
 } trtv_geom;
 
 /* Human-readable name of a status code (static storage). */

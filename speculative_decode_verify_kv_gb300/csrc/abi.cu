@@ -97,7 +97,7 @@ trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
   if (g == nullptr) return TRTV_ERR_INVALID_ARG;
   if (g->batch < 1 || g->qo_len < 1 || g->num_q_heads < 1 || g->num_kv_heads < 1 ||
       g->num_q_heads % g->num_kv_heads != 0 || g->max_pages_per_req < 1 || g->num_slots < 1 ||
-      g->slot_stride < 2 || g->num_ctas < 0)
+      g->slot_stride < 2 || g->num_ctas < 0 || g->num_ctas > kMaxCombineParts)
     return TRTV_ERR_INVALID_ARG;
   if (g->kv_dtype != TRTV_BF16 && g->kv_dtype != TRTV_FP8_E4M3) return TRTV_ERR_INVALID_ARG;
   if (!(g->sm_scale > 0.f) || !(g->k_scale > 0.f) || !std::isfinite(g->sm_scale) ||

@@ -24,6 +24,7 @@ constexpr int kGroups = 4;        // sub-pages per page
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kBox = 4096;        // bytes of one TMA box: 32 rows x 128 B
+constexpr int kMaxCombineParts = 1024;  // upper bound on num_ctas
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
 
 // ---- parameter blocks ----------------------------------------------------

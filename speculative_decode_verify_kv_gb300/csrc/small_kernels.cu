@@ -102,29 +102,65 @@ __global__ void combine_kernel(CombineParams p) {
   const int64_t P = p.num_ctas;
   const int64_t c0 = cta_of_unit(start, W, P), c1 = cta_of_unit(start + units - 1, W, P);
   if (c0 == c1) return;  // one CTA wrote the final rows
+  // partial slots of this sequence, in CTA order (64-bit divisions only here)
+  __shared__ int s_slot[kMaxCombineParts];
+  __shared__ int s_wcnt[32];
+  __shared__ int s_np;
+  __shared__ float s_m[128], s_inv[128];
+  if (threadIdx.x == 0) s_np = 0;
+  __syncthreads();
+  const int64_t ncand = c1 - c0 + 1;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int64_t i0 = 0; i0 < ncand; i0 += blockDim.x) {
+    const int64_t i = i0 + threadIdx.x;
+    bool has = false;
+    int slot = 0;
+    if (i < ncand) {
+      const int64_t c = c0 + i;
+      const int64_t cb = cta_unit_begin(c, W, P), ce = cta_unit_begin(c + 1, W, P);
+      has = cb < ce;
+      slot = static_cast<int>(2 * c + (cb >= start ? 0 : 1));
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) s_wcnt[wid] = __popc(bal);
+    __syncthreads();
+    int base = s_np;
+    for (int w = 0; w < wid; ++w) base += s_wcnt[w];
+    if (has) s_slot[base + __popc(bal & ((1u << lane) - 1u))] = slot;  // CTA order kept
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int add = 0;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) add += s_wcnt[w];
+      s_np += add;
+    }
+    __syncthreads();
+  }
+  const int np = s_np;
+  // per row: maximum log2-sum-exp and the normaliser
+  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int i = 0; i < np; ++i) M = fmaxf(M, p.ws_lse[static_cast<int64_t>(s_slot[i]) * p.rows_pad + r]);
+    float den = 0.f;
+    if (M != -INFINITY)
+      for (int i = 0; i < np; ++i) den += exp2f(p.ws_lse[static_cast<int64_t>(s_slot[i]) * p.rows_pad + r] - M);
+    s_m[r] = M;
+    s_inv[r] = den > 0.f ? p.v_scale / den : 0.f;
+  }
+  __syncthreads();
   for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
     const int r = e / D, d = e % D;
     const int t = r / p.group_pad, gl = r % p.group_pad;
     if (t >= T || gl >= p.group) continue;
-    float M = -INFINITY;
-    for (int64_t c = c0; c <= c1; ++c) {
-      const int64_t cb = cta_unit_begin(c, W, P), ce = cta_unit_begin(c + 1, W, P);
-      if (cb >= ce) continue;
-      const int64_t slot = 2 * c + (cb >= start ? 0 : 1);
-      M = fmaxf(M, p.ws_lse[slot * p.rows_pad + r]);
-    }
-    float num = 0.f, den = 0.f;
+    const float M = s_m[r];
+    float num = 0.f;
     if (M != -INFINITY) {
-      for (int64_t c = c0; c <= c1; ++c) {
-        const int64_t cb = cta_unit_begin(c, W, P), ce = cta_unit_begin(c + 1, W, P);
-        if (cb >= ce) continue;
-        const int64_t slot = 2 * c + (cb >= start ? 0 : 1);
-        const float w = exp2f(p.ws_lse[slot * p.rows_pad + r] - M);
-        num += w * p.ws_o[(slot * p.rows_pad + r) * D + d];
-        den += w;
+      for (int i = 0; i < np; ++i) {
+        const int64_t sl = s_slot[i];
+        const float w = exp2f(p.ws_lse[sl * p.rows_pad + r] - M);
+        num += w * p.ws_o[(sl * p.rows_pad + r) * D + d];
       }
     }
-    const float v = den > 0.f ? num / den * p.v_scale : 0.f;
+    const float v = num * s_inv[r];
     const int64_t o = ((static_cast<int64_t>(b) * T + t) * p.num_q_heads + h * p.group + gl) * D + d;
     if (p.out_f32) static_cast<float*>(p.out)[o] = v;
     else static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16(v);
