@@ -4,7 +4,7 @@ Headline workload ("dense"): batch 64, qo_len 4, kv_len ~ U{1024..8192},
 32 query / 4 KV heads, head_dim 128, bf16 K/V in P128 pages read through the
 P32 grouped-HND view, bf16 output.  One step = one verify pass of that batch:
 the P32 sub-page view (trtv_subpage_view) and the dense ladder attention with
-its split-KV combine (trtv_verify_dense).  The MSA sparse pass (proxy scores
+its split-KV merge (trtv_verify_dense).  The MSA sparse pass (proxy scores
 -> per-token top-k -> sparse attention) is timed the same way on the "msa"
 workload (batch 32, kv_len ~ U{16384..65536}, 64 / 4 heads, top-k 16) and
 reported under "paths".
@@ -12,7 +12,7 @@ reported under "paths".
 value      query tokens per second (batch * qo_len per step), whole job
 e2e        the same through the C ABI with per-step host->device copies of
            q / page table / kv_lens from pinned memory and the output read back
-roofline   the dominant call (trtv_verify_dense: attention + combine) against
+roofline   the dominant call (trtv_verify_dense: one attn_kernel launch) against
            the measured HBM copy bandwidth; algorithmic bytes = K and V of
            every visible position + Q + O
 cpu_baseline  the fp64 oracle on a bounded sample of the same workload
@@ -209,10 +209,10 @@ def time_path(name, steps, warmup, sampler=None):
     msa = p.topk > 0
     if msa:
         calls = [("proxy", dv.proxy), ("topk", dv.select), ("sparse", dv.sparse)]
-        launches = 5   # proxy, topk, plan, attention, combine
+        launches = 4   # proxy, topk, sparse plan, attention (merge in-kernel)
     else:
         calls = [("subpage_view", dv.subpage_view), ("verify_dense", dv.dense)]
-        launches = 3   # sub-page view, attention, combine
+        launches = 2   # sub-page view, attention (merge in-kernel)
     for _ in range(warmup):
         for _, f in calls:
             f()
@@ -428,7 +428,7 @@ def main():
     dom_bytes = head["bytes"][dom]
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     step_bytes = sum(head["bytes"].values())
-    kernel_name = "proxy_kernel" if p.topk else "attn_kernel+combine_kernel"
+    kernel_name = "proxy_kernel" if p.topk else "attn_kernel"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": ncu_traffic(dom, args.workload),
                 "kernel": f"{dom} ({kernel_name})", "peak_kind": f"of {peak_kind}",

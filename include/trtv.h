@@ -79,6 +79,7 @@ typedef enum { TRTV_BF16 = 0, TRTV_FP8_E4M3 = 1, TRTV_F32 = 2 } trtv_dtype;
 #define TRTV_DEVERR_KV_LEN 1    /* kv_len < qo_len or kv_len > 128 * max_pages */
 #define TRTV_DEVERR_PAGE_ID 2   /* a used page-table entry outside [0, num_slots) */
 #define TRTV_DEVERR_BLOCK_IDX 4 /* a top-k block index >= max_pages_per_req */
+#define TRTV_DEVERR_TIMEOUT 8   /* a pipeline wait gave up after 2 s (results invalid) */
 
 typedef struct {
   int32_t batch;             /* requests B >= 1 */
@@ -124,9 +125,12 @@ trtv_status trtv_subpage_view(const trtv_geom* geom, const int32_t* page_table,
 
 /*
  * Workspace bytes that trtv_verify_dense and trtv_msa_sparse_attn need for
- * this geometry (topk = the sparse path's k, 0 for dense only).  The
- * workspace is caller-allocated device memory, 256-byte aligned, reusable
- * across calls (no initialisation needed); 0 on invalid geometry.
+ * this geometry (topk = the sparse path's k, 0 for dense only); 0 on invalid
+ * geometry.  The workspace is caller-allocated device memory, 256-byte
+ * aligned.  Zero-fill it once before its first use (it holds the arrival
+ * counters of sequences split across CTAs); every call that completes leaves
+ * it zeroed again, so it is reused without further initialisation.  After a
+ * call that reported TRTV_DEVERR_TIMEOUT, zero it again.
  */
 size_t trtv_workspace_bytes(const trtv_geom* geom, int32_t topk);
 
@@ -135,8 +139,9 @@ size_t trtv_workspace_bytes(const trtv_geom* geom, int32_t topk);
  * layers' ladder SDPA mask, identical to decode at qo_len = 1).
  * out[b*T + t][hq][:] = sum_{p <= L_b - T + t} softmax_p(x) v_p, with
  *   x_p = sm_scale * k_scale * (q[b*T + t][hq] . k_p),  v_p scaled by v_scale,
- * k_p / v_p from KV head hq / G of request b.  Split-KV across CTAs with a
- * log-sum-exp combine; fp32 accumulation.  out_dtype: TRTV_BF16 or TRTV_F32.
+ * k_p / v_p from KV head hq / G of request b.  Split-KV across CTAs with an
+ * in-kernel log-sum-exp merge; fp32 accumulation.  out_dtype: TRTV_BF16 or
+ * TRTV_F32.
  */
 trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* kv_pool,
                               const int32_t* page_table, const int32_t* kv_lens, void* out,

@@ -89,7 +89,7 @@ struct Plan {
   int group, group_pad, rows, mt, rows_pad, num_ctas, n_seq;
   int64_t pool_rows;
   // workspace
-  size_t ws_o, ws_lse, ws_blocks, ws_masks, ws_count, ws_total;
+  size_t ws_o, ws_lse, ws_counters, ws_blocks, ws_masks, ws_count, ws_total;
   int plan_cap;
 };
 
@@ -127,6 +127,8 @@ trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
   off = align_up(off + P2 * p.rows_pad * g->head_dim * sizeof(float), 256);
   p.ws_lse = off;
   off = align_up(off + P2 * p.rows_pad * sizeof(float), 256);
+  p.ws_counters = off;
+  off = align_up(off + static_cast<size_t>(ctas) * sizeof(int), 256);
   p.plan_cap = topk > 0 ? std::min(g->qo_len * topk, g->max_pages_per_req) : 0;
   p.ws_blocks = off;
   off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(int32_t), 256);
@@ -251,6 +253,7 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   a.out = out;
   a.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
   a.ws_lse = reinterpret_cast<float*>(wsb + pl.ws_lse);
+  a.counters = reinterpret_cast<int*>(wsb + pl.ws_counters);
   a.plan_blocks = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_blocks) : nullptr;
   a.plan_masks = sparse ? reinterpret_cast<const uint32_t*>(wsb + pl.ws_masks) : nullptr;
   a.plan_count = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_count) : nullptr;
@@ -285,27 +288,6 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   e = g->kv_dtype == TRTV_FP8_E4M3
           ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
           : launch_attn_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
-  if (e != cudaSuccess) return TRTV_ERR_CUDA;
-  CombineParams cp{};
-  cp.kv_lens = lens;
-  cp.plan_count = a.plan_count;
-  cp.ws_o = a.ws_o;
-  cp.ws_lse = a.ws_lse;
-  cp.out = out;
-  cp.batch = g->batch;
-  cp.qo_len = g->qo_len;
-  cp.num_q_heads = g->num_q_heads;
-  cp.num_kv_heads = g->num_kv_heads;
-  cp.group = pl.group;
-  cp.group_pad = pl.group_pad;
-  cp.head_dim = g->head_dim;
-  cp.max_pages = g->max_pages_per_req;
-  cp.rows_pad = pl.rows_pad;
-  cp.sparse = a.sparse;
-  cp.out_f32 = a.out_f32;
-  cp.num_ctas = pl.num_ctas;
-  cp.v_scale = g->v_scale;
-  e = launch_combine(cp, pl.n_seq, st);
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
 }
 

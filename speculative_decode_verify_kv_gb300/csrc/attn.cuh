@@ -13,7 +13,7 @@
 // concatenated in sequence order; CTA c takes units [c W / P, (c+1) W / P).
 // A sequence that one CTA covers whole is written as final output; the
 // pieces of a cut sequence are written as (normalised output, log2-sum-exp)
-// partials and merged by combine_kernel.
+// partials and merged by the contributor that finishes last (merge_if_last).
 //
 // Roles: warp 8 issues TMA tiled loads of each page's K and V sub-pages
 // (128B swizzle) into an NST-stage ring guarded by full/empty mbarriers.
@@ -132,6 +132,98 @@ __device__ __forceinline__ void cursor_next(SeqCursor& cur, const int32_t* scan,
   if ((sparse ? cur.s : cur.b) < n) cursor_fill(cur, scan, Hk, sparse);
 }
 
+// Split-KV merge inside the attention kernel.  A sequence cut between CTAs
+// c_first .. c_last leaves one (normalised output, log2-sum-exp) partial per
+// CTA; each contributor, after writing its partial, counts itself in
+// counters[c_last] (c_last's range starts inside the sequence, so the slot is
+// unique per cut sequence).  The contributor that completes the count merges
+// the partials in CTA order (fixed summation order) -- o = sum_i 2^(lse_i - M)
+// o_i / sum_i 2^(lse_i - M) -- writes the rows and resets the counter to zero,
+// leaving the workspace ready for the next call.  Executed by the 256
+// consumer threads.
+template <int D>
+__device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t W, float* mlf,
+                              int* flag) {
+  const int tid = threadIdx.x;
+  const int64_t P = p.num_ctas;
+  named_barrier(1, kConsumerWarps * 32);  // this CTA's partial rows are written
+  if (tid == 0) {
+    const int64_t c_first = cta_of_unit(cur.start, W, P);
+    const int64_t c_last = cta_of_unit(cur.start + cur.units - 1, W, P);
+    int n = 0;
+    if (W >= P) {
+      n = static_cast<int>(c_last - c_first + 1);  // every CTA range is non-empty
+    } else {
+      for (int64_t c = c_first; c <= c_last; ++c)
+        n += cta_unit_begin(c, W, P) < cta_unit_begin(c + 1, W, P);
+    }
+    __threadfence();
+    const int old = atomicAdd(&p.counters[c_last], 1);
+    const int last = old == n - 1;
+    if (last) __threadfence();
+    flag[0] = last;
+    flag[1] = static_cast<int>(c_first);
+    flag[2] = static_cast<int>(c_last);
+    flag[3] = cta_unit_begin(c_first, W, P) < cur.start ? 1 : 0;  // slot of the first piece
+  }
+  named_barrier(1, kConsumerWarps * 32);
+  if (!flag[0]) return;
+  const int c_first = flag[1], c_last = flag[2], first_off = flag[3];
+  const bool all_ranges = W >= P;
+  auto slot_of = [&](int c, bool& used) -> int64_t {
+    used = all_ranges || cta_unit_begin(c, W, P) < cta_unit_begin(c + 1, W, P);
+    return 2 * static_cast<int64_t>(c) + (c == c_first ? first_off : 0);
+  };
+  for (int r = tid; r < p.rows_pad; r += kConsumerWarps * 32) {
+    float M = -INFINITY;
+    for (int c = c_first; c <= c_last; ++c) {
+      bool used;
+      const int64_t sl = slot_of(c, used);
+      if (used) M = fmaxf(M, __ldcg(p.ws_lse + sl * p.rows_pad + r));
+    }
+    float den = 0.f;
+    if (M != -INFINITY)
+      for (int c = c_first; c <= c_last; ++c) {
+        bool used;
+        const int64_t sl = slot_of(c, used);
+        if (used) den += exp2f(__ldcg(p.ws_lse + sl * p.rows_pad + r) - M);
+      }
+    mlf[2 * r] = M;
+    mlf[2 * r + 1] = den > 0.f ? p.v_scale / den : 0.f;
+  }
+  named_barrier(1, kConsumerWarps * 32);
+  const int64_t obase = static_cast<int64_t>(cur.b) * p.qo_len;
+  for (int e = tid; e < p.rows_pad * (D / 4); e += kConsumerWarps * 32) {
+    const int r = e / (D / 4), d = 4 * (e % (D / 4));
+    const int t = r / p.group_pad, gl = r % p.group_pad;
+    if (t >= p.qo_len || gl >= p.group) continue;
+    const float M = mlf[2 * r], inv = mlf[2 * r + 1];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int c = c_first; c <= c_last; ++c) {
+        bool used;
+        const int64_t sl = slot_of(c, used);
+        if (!used) continue;
+        const float w = exp2f(__ldcg(p.ws_lse + sl * p.rows_pad + r) - M);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * p.rows_pad + r) * D + d));
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      }
+    }
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(cur.h) * p.group + gl) * D + d;
+    if (p.out_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) = acc;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow) = pk;
+    }
+  }
+  if (tid == 0) atomicExch(&p.counters[c_last], 0);
+}
+
 template <bool FP8, int D, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ AttnParams p) {
@@ -177,6 +269,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     return 0;
   });
   const int64_t W = item_start(scan, nitems, Hk, sparse);
+  // rows of sequences with no units (invalid request, or no selected block)
+  // are zero: CTA c clears items c, c + P, ...
+  for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+    if (scan[i + 1] != scan[i]) continue;
+    const int b = sparse ? i / Hk : i;
+    const int h0 = sparse ? i % Hk : 0, nh = sparse ? 1 : Hk;
+    const int span = nh * p.group * D;  // contiguous query heads of these KV heads
+    for (int t = 0; t < T; ++t) {
+      const int64_t o0 = ((static_cast<int64_t>(b) * T + t) * p.num_q_heads +
+                          static_cast<int64_t>(h0) * p.group) * D;
+      for (int e = threadIdx.x; e < span; e += blockDim.x) {
+        if (p.out_f32) static_cast<float*>(p.out)[o0 + e] = 0.f;
+        else static_cast<__nv_bfloat16*>(p.out)[o0 + e] = __float2bfloat16(0.f);
+      }
+    }
+  }
   if (W == 0) return;
   const int64_t u0 = cta_unit_begin(blockIdx.x, W, p.num_ctas);
   const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);
@@ -532,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_barrier(1, kConsumerWarps * 32);
       }
     }
+    if (!whole) merge_if_last<D>(p, cur, W, mlf, reinterpret_cast<int*>(ml));
   }
 }
 

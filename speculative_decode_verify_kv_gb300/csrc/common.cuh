@@ -13,8 +13,6 @@
 
 #include "../../include/trtv.h"
 
-// A wait that gives up sets this bit; the kernel then drains and returns.
-#define TRTV_DEVERR_TIMEOUT 8
 
 namespace trtv {
 
@@ -36,6 +34,7 @@ struct AttnParams {
   void* out;
   float* ws_o;          // [2 * num_ctas, rows_pad, D] partial outputs
   float* ws_lse;        // [2 * num_ctas, rows_pad] partial log2-sum-exp
+  int* counters;        // [num_ctas] arrivals per cut sequence, zero between calls
   const int32_t* plan_blocks;   // sparse: [n_seq, plan_cap] selected blocks
   const uint32_t* plan_masks;   // sparse: [n_seq, plan_cap] token bitmasks
   const int32_t* plan_count;    // sparse: [n_seq]
@@ -59,17 +58,6 @@ struct ProxyParams {
   int max_pages, num_slots, slot_stride, rows, rows_pad, num_ctas, nstages;
   float score_scale;    // sm_scale * k_scale (> 0, so it commutes with max)
   int off_stage, stage_bytes, off_red, off_scan, off_bar;
-};
-
-struct CombineParams {
-  const int32_t* kv_lens;
-  const int32_t* plan_count;
-  const float* ws_o;
-  const float* ws_lse;
-  void* out;
-  int batch, qo_len, num_q_heads, num_kv_heads, group, group_pad, head_dim;
-  int max_pages, rows_pad, sparse, out_f32, num_ctas;
-  float v_scale;
 };
 
 // ---- small helpers -------------------------------------------------------
@@ -224,7 +212,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// ---- work split (shared by the attention, proxy and combine kernels) ------
+// ---- work split (shared by the attention and proxy kernels) ----------------
 
 // Units of work of a CTA: [floor(c W / P), floor((c+1) W / P)).
 __device__ __forceinline__ int64_t cta_unit_begin(int64_t c, int64_t W, int64_t P) {

@@ -9,7 +9,6 @@ namespace trtv {
 
 struct AttnParams;
 struct ProxyParams;
-struct CombineParams;
 
 // attention: head_dim in {64, 128}; mt (row tiles of 16) in {1, 2, 4, 8}
 cudaError_t launch_attn_bf16(int head_dim, int mt, const CUtensorMap& map, const AttnParams& p,
@@ -24,7 +23,6 @@ cudaError_t launch_proxy_fp8(int head_dim, int mt, const CUtensorMap& map, const
 cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t* k_sub,
                                 int32_t* v_sub, int batch, int qo_len, int max_pages,
                                 int num_slots, int stride, int* err, cudaStream_t st);
-cudaError_t launch_combine(const CombineParams& p, int n_seq, cudaStream_t st);
 cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
                                int num_kv_heads, int max_pages, int topk, int plan_cap,
                                int32_t* plan_blocks, uint32_t* plan_masks, int32_t* plan_count,

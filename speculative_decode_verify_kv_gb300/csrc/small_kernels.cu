@@ -1,6 +1,5 @@
 // small_kernels.cu -- the latency-bound kernels of the verify path:
 //   subpage_view_kernel   P128 page table -> P32 grouped-HND sub-page indices
-//   combine_kernel        log-sum-exp merge of split-KV partials
 //   sparse_plan_kernel    per (request, KV head): unique selected blocks and
 //                         the bitmask of verify tokens that selected each
 //   topk_kernel           warp-level per-token top-k (radix select), ties to
@@ -36,134 +35,6 @@ __global__ void subpage_view_kernel(const int32_t* __restrict__ pt, const int32_
     const int gi = j % kGroups;
     k_sub[e] = static_cast<int32_t>(kGroups * (s * stride) + gi);
     v_sub[e] = static_cast<int32_t>(kGroups * (s * stride + 1) + gi);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Split-KV combine: for every (request, KV head) sequence cut across CTAs,
-// o = sum_i 2^(lse_i - M) o_i / sum_i 2^(lse_i - M), M = max_i lse_i; every
-// sequence with no units (invalid request, or nothing selected) is zeroed.
-__global__ void combine_kernel(CombineParams p) {
-  const int s = blockIdx.x;
-  const int Hk = p.num_kv_heads, T = p.qo_len, D = p.head_dim;
-  const int b = s / Hk, h = s % Hk;
-  const int n = p.sparse ? p.batch * Hk : p.batch;
-  __shared__ int64_t red[2][32];
-  int64_t before = 0, total = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    int64_t u;
-    if (p.sparse) {
-      u = p.plan_count[i];
-    } else {
-      const int L = p.kv_lens[i];
-      u = len_valid(L, T, p.max_pages) ? (L + kPage - 1) / kPage : 0;
-    }
-    total += u;
-    if (i < (p.sparse ? s : b)) before += u;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    total += __shfl_xor_sync(0xffffffffu, total, o);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = before;
-    red[1][threadIdx.x >> 5] = total;
-  }
-  __syncthreads();
-  before = total = 0;
-  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
-    before += red[0][w];
-    total += red[1][w];
-  }
-  int64_t start, units, W;
-  if (p.sparse) {
-    start = before;
-    units = p.plan_count[s];
-    W = total;
-  } else {
-    const int L = p.kv_lens[b];
-    units = len_valid(L, T, p.max_pages) ? (L + kPage - 1) / kPage : 0;
-    start = before * Hk + h * units;
-    W = total * Hk;
-  }
-  const int rows = p.group_pad * T;
-  if (units == 0) {
-    for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
-      const int r = e / D, d = e % D;
-      const int t = r / p.group_pad, gl = r % p.group_pad;
-      if (t >= T || gl >= p.group) continue;
-      const int64_t o = ((static_cast<int64_t>(b) * T + t) * p.num_q_heads + h * p.group + gl) * D + d;
-      if (p.out_f32) static_cast<float*>(p.out)[o] = 0.f;
-      else static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16(0.f);
-    }
-    return;
-  }
-  const int64_t P = p.num_ctas;
-  const int64_t c0 = cta_of_unit(start, W, P), c1 = cta_of_unit(start + units - 1, W, P);
-  if (c0 == c1) return;  // one CTA wrote the final rows
-  // partial slots of this sequence, in CTA order (64-bit divisions only here)
-  __shared__ int s_slot[kMaxCombineParts];
-  __shared__ int s_wcnt[32];
-  __shared__ int s_np;
-  __shared__ float s_m[128], s_inv[128];
-  if (threadIdx.x == 0) s_np = 0;
-  __syncthreads();
-  const int64_t ncand = c1 - c0 + 1;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int64_t i0 = 0; i0 < ncand; i0 += blockDim.x) {
-    const int64_t i = i0 + threadIdx.x;
-    bool has = false;
-    int slot = 0;
-    if (i < ncand) {
-      const int64_t c = c0 + i;
-      const int64_t cb = cta_unit_begin(c, W, P), ce = cta_unit_begin(c + 1, W, P);
-      has = cb < ce;
-      slot = static_cast<int>(2 * c + (cb >= start ? 0 : 1));
-    }
-    const unsigned bal = __ballot_sync(0xffffffffu, has);
-    if (lane == 0) s_wcnt[wid] = __popc(bal);
-    __syncthreads();
-    int base = s_np;
-    for (int w = 0; w < wid; ++w) base += s_wcnt[w];
-    if (has) s_slot[base + __popc(bal & ((1u << lane) - 1u))] = slot;  // CTA order kept
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int add = 0;
-      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) add += s_wcnt[w];
-      s_np += add;
-    }
-    __syncthreads();
-  }
-  const int np = s_np;
-  // per row: maximum log2-sum-exp and the normaliser
-  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-    float M = -INFINITY;
-    for (int i = 0; i < np; ++i) M = fmaxf(M, p.ws_lse[static_cast<int64_t>(s_slot[i]) * p.rows_pad + r]);
-    float den = 0.f;
-    if (M != -INFINITY)
-      for (int i = 0; i < np; ++i) den += exp2f(p.ws_lse[static_cast<int64_t>(s_slot[i]) * p.rows_pad + r] - M);
-    s_m[r] = M;
-    s_inv[r] = den > 0.f ? p.v_scale / den : 0.f;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
-    const int r = e / D, d = e % D;
-    const int t = r / p.group_pad, gl = r % p.group_pad;
-    if (t >= T || gl >= p.group) continue;
-    const float M = s_m[r];
-    float num = 0.f;
-    if (M != -INFINITY) {
-      for (int i = 0; i < np; ++i) {
-        const int64_t sl = s_slot[i];
-        const float w = exp2f(p.ws_lse[sl * p.rows_pad + r] - M);
-        num += w * p.ws_o[(sl * p.rows_pad + r) * D + d];
-      }
-    }
-    const float v = num * s_inv[r];
-    const int64_t o = ((static_cast<int64_t>(b) * T + t) * p.num_q_heads + h * p.group + gl) * D + d;
-    if (p.out_f32) static_cast<float*>(p.out)[o] = v;
-    else static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16(v);
   }
 }
 
@@ -356,11 +227,6 @@ cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t*
   const int blocks = static_cast<int>(want < 4096 ? (want > 0 ? want : 1) : 4096);
   subpage_view_kernel<<<blocks, threads, 0, st>>>(pt, lens, k_sub, v_sub, batch, qo_len, max_pages,
                                                   num_slots, stride, err);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const CombineParams& p, int n_seq, cudaStream_t st) {
-  combine_kernel<<<n_seq, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
