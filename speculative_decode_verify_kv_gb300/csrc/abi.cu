@@ -197,6 +197,53 @@ bool plan_attn_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams*
   return *bytes <= kSmemOptin;
 }
 
+// 3-D view of q [B*T][Hq][D] for the tcgen05 proxy's Q tiles: box [T][G][64].
+bool encode_q_map(const trtv_geom* g, const Plan& pl, const void* q, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(g->head_dim), static_cast<cuuint64_t>(g->num_q_heads),
+                        static_cast<cuuint64_t>(g->batch) * g->qo_len};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(g->head_dim) * 2,
+                           static_cast<cuuint64_t>(g->num_q_heads) * g->head_dim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pl.group), static_cast<cuuint32_t>(g->qo_len)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The tcgen05 proxy covers bf16, head_dim 128, a power-of-two group <= 16 with
+// group * qo_len <= 128 rows (one UMMA M = 128 tile).
+bool proxy_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
+  return g->kv_dtype == TRTV_BF16 && g->head_dim == 128 && pl.group == pl.group_pad &&
+         pl.group <= 16 && pl.group * g->qo_len <= 128 && aligned(q, 16);
+}
+
+bool plan_proxy_umma_smem(const trtv_geom* g, ProxyParams* a, size_t* bytes) {
+  const size_t qbufs = 2 * 128 * 128 * 2;
+  const size_t stage = static_cast<size_t>(kGroups) * 2 * kBox;
+  const size_t scan = align_up((static_cast<size_t>(g->batch) + 1 + 32) * sizeof(int32_t), 16);
+  const size_t budget = kSmemOptin - kAlignSlack - 1024;
+  const size_t fixed = qbufs + scan + (2 * 8 + 9) * sizeof(uint64_t) + 16;
+  if (fixed + 2 * stage > budget) return false;
+  int nst = static_cast<int>((budget - fixed) / stage);
+  if (nst > 6) nst = 6;
+  a->off_q = 0;
+  a->off_stage = static_cast<int>(qbufs);
+  a->stage_bytes = static_cast<int>(stage);
+  size_t off = qbufs + static_cast<size_t>(nst) * stage;
+  a->off_red = 0;
+  a->off_scan = static_cast<int>(off);
+  off += scan;
+  a->off_bar = static_cast<int>(align_up(off, 8));
+  off = a->off_bar + (2 * nst + 9) * sizeof(uint64_t) + 16;
+  a->nstages = nst;
+  *bytes = off + kAlignSlack;
+  return *bytes <= kSmemOptin - 1024;
+}
+
 bool plan_proxy_smem(const trtv_geom* g, const Plan& pl, ProxyParams* a, size_t* bytes) {
   const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
   const int NB = fp8 ? 1 : g->head_dim * 2 / 128;
@@ -387,9 +434,12 @@ trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* 
   if (err == nullptr) return TRTV_ERR_CUDA;
   ProxyParams a{};
   size_t smem = 0;
-  if (!plan_proxy_smem(g, pl, &a, &smem)) return TRTV_ERR_UNSUPPORTED;
-  CUtensorMap map;
+  const bool umma = proxy_umma_eligible(g, pl, q);
+  if (umma ? !plan_proxy_umma_smem(g, &a, &smem) : !plan_proxy_smem(g, pl, &a, &smem))
+    return TRTV_ERR_UNSUPPORTED;
+  CUtensorMap map, qmap;
   if (!encode_pool_map(g, pl, kv_pool, &map)) return TRTV_ERR_CUDA;
+  if (umma && !encode_q_map(g, pl, q, &qmap)) return TRTV_ERR_CUDA;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.page_table = page_table;
   a.kv_lens = kv_lens;
@@ -410,9 +460,11 @@ trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* 
   a.num_ctas = pl.num_ctas;
   a.score_scale = g->sm_scale * g->k_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = g->kv_dtype == TRTV_FP8_E4M3
-                            ? launch_proxy_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
-                            : launch_proxy_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  const cudaError_t e =
+      umma ? launch_proxy_umma(map, qmap, a, pl.num_ctas, smem, st)
+           : g->kv_dtype == TRTV_FP8_E4M3
+                 ? launch_proxy_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
+                 : launch_proxy_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
 }
 

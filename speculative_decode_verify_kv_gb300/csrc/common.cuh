@@ -58,6 +58,7 @@ struct ProxyParams {
   int max_pages, num_slots, slot_stride, rows, rows_pad, num_ctas, nstages;
   float score_scale;    // sm_scale * k_scale (> 0, so it commutes with max)
   int off_stage, stage_bytes, off_red, off_scan, off_bar;
+  int off_q;            // tcgen05 path: two Q tiles of 128 rows x 128 bf16
 };
 
 // ---- small helpers -------------------------------------------------------

@@ -20,6 +20,10 @@ cudaError_t launch_proxy_bf16(int head_dim, int mt, const CUtensorMap& map, cons
 cudaError_t launch_proxy_fp8(int head_dim, int mt, const CUtensorMap& map, const ProxyParams& p,
                              int grid, size_t smem, cudaStream_t st);
 
+// tcgen05 proxy: bf16, head_dim 128, power-of-two group <= 16, group * qo_len <= 128
+cudaError_t launch_proxy_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const ProxyParams& p,
+                              int grid, size_t smem, cudaStream_t st);
+
 cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t* k_sub,
                                 int32_t* v_sub, int batch, int qo_len, int max_pages,
                                 int num_slots, int stride, int* err, cudaStream_t st);

@@ -1,5 +1,6 @@
-// proxy_bf16.cu -- instantiations of the proxy kernel for bf16 KV caches.
+// proxy_bf16.cu -- instantiations of the proxy kernels (mma.sync and tcgen05) for bf16 KV caches.
 #include "proxy.cuh"
+#include "proxy_umma.cuh"
 #include "launch.h"
 
 namespace trtv {
@@ -32,6 +33,15 @@ cudaError_t launch_proxy_bf16(int head_dim, int mt, const CUtensorMap& map, cons
     }
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_proxy_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const ProxyParams& p,
+                              int grid, size_t smem, cudaStream_t st) {
+  const void* fn = reinterpret_cast<const void*>(&proxy_umma_kernel<128>);
+  cudaError_t e = ensure_smem_attr(fn, smem);
+  if (e != cudaSuccess) return e;
+  proxy_umma_kernel<128><<<grid, kUmmaProxyThreads, smem, st>>>(kv_map, q_map, p);
+  return cudaGetLastError();
 }
 
 }  // namespace trtv
