@@ -214,6 +214,40 @@ bool encode_q_map(const trtv_geom* g, const Plan& pl, const void* q, CUtensorMap
   return r == CUDA_SUCCESS;
 }
 
+// The tcgen05 attention kernel covers bf16, head_dim 128 and a power-of-two
+// group with group * qo_len <= 128 rows (one UMMA M = 128 tile).
+bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
+  return g->kv_dtype == TRTV_BF16 && g->head_dim == 128 && pl.group == pl.group_pad &&
+         pl.group * g->qo_len <= 128 && aligned(q, 16);
+}
+
+bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
+  const size_t qbufs = 2 * 128 * 128 * 2;
+  const size_t kv = static_cast<size_t>(kGroups) * 2 * kBox;
+  const int nitems = sparse ? pl.n_seq : g->batch;
+  const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
+  const size_t ml = 512 * sizeof(float);
+  const int nk = 2, nv = 2;
+  size_t off = qbufs;
+  a->off_q = 0;
+  a->off_stage = static_cast<int>(off);
+  a->stage_bytes = static_cast<int>(kv);
+  off += nk * kv;
+  a->off_vring = static_cast<int>(off);
+  off += nv * kv;
+  a->off_scan = static_cast<int>(off);
+  off += scan;
+  a->off_ml = static_cast<int>(off);
+  off += ml;
+  a->off_bar = static_cast<int>(align_up(off, 8));
+  off = a->off_bar + (2 * nk + 2 * nv + 11) * sizeof(uint64_t) + 16;
+  a->nstages = nk;
+  a->nv = nv;
+  a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
+  *bytes = off + kAlignSlack;
+  return *bytes <= kSmemOptin;
+}
+
 // The tcgen05 proxy covers bf16, head_dim 128, a power-of-two group <= 16 with
 // group * qo_len <= 128 rows (one UMMA M = 128 tile).
 bool proxy_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
@@ -289,9 +323,12 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   if (err == nullptr) return TRTV_ERR_CUDA;
   AttnParams a{};
   size_t smem = 0;
-  if (!plan_attn_smem(g, pl, sparse, &a, &smem)) return TRTV_ERR_UNSUPPORTED;
-  CUtensorMap map;
+  const bool umma = attn_umma_eligible(g, pl, q);
+  if (umma ? !plan_attn_umma_smem(g, pl, sparse, &a, &smem) : !plan_attn_smem(g, pl, sparse, &a, &smem))
+    return TRTV_ERR_UNSUPPORTED;
+  CUtensorMap map, qmap;
   if (!encode_pool_map(g, pl, pool, &map)) return TRTV_ERR_CUDA;
+  if (umma && !encode_q_map(g, pl, q, &qmap)) return TRTV_ERR_CUDA;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -332,9 +369,10 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
                            reinterpret_cast<int32_t*>(wsb + pl.ws_count), err, st);
     if (e != cudaSuccess) return TRTV_ERR_CUDA;
   }
-  e = g->kv_dtype == TRTV_FP8_E4M3
-          ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
-          : launch_attn_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  e = umma ? launch_attn_umma(map, qmap, a, pl.num_ctas, smem, st)
+       : g->kv_dtype == TRTV_FP8_E4M3
+           ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
+           : launch_attn_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
 }
 

@@ -139,14 +139,14 @@ __device__ __forceinline__ void cursor_next(SeqCursor& cur, const int32_t* scan,
 // unique per cut sequence).  The contributor that completes the count merges
 // the partials in CTA order (fixed summation order) -- o = sum_i 2^(lse_i - M)
 // o_i / sum_i 2^(lse_i - M) -- writes the rows and resets the counter to zero,
-// leaving the workspace ready for the next call.  Executed by the 256
-// consumer threads.
-template <int D>
+// leaving the workspace ready for the next call.  Executed by the NTHR
+// threads with threadIdx.x < NTHR, which synchronise on named barrier 1.
+template <int D, int NTHR = kConsumerWarps * 32>
 __device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t W, float* mlf,
                               int* flag) {
   const int tid = threadIdx.x;
   const int64_t P = p.num_ctas;
-  named_barrier(1, kConsumerWarps * 32);  // this CTA's partial rows are written
+  named_barrier(1, NTHR);  // this CTA's partial rows are written
   if (tid == 0) {
     const int64_t c_first = cta_of_unit(cur.start, W, P);
     const int64_t c_last = cta_of_unit(cur.start + cur.units - 1, W, P);
@@ -166,7 +166,7 @@ __device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t
     flag[2] = static_cast<int>(c_last);
     flag[3] = cta_unit_begin(c_first, W, P) < cur.start ? 1 : 0;  // slot of the first piece
   }
-  named_barrier(1, kConsumerWarps * 32);
+  named_barrier(1, NTHR);
   if (!flag[0]) return;
   const int c_first = flag[1], c_last = flag[2], first_off = flag[3];
   const bool all_ranges = W >= P;
@@ -174,7 +174,7 @@ __device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t
     used = all_ranges || cta_unit_begin(c, W, P) < cta_unit_begin(c + 1, W, P);
     return 2 * static_cast<int64_t>(c) + (c == c_first ? first_off : 0);
   };
-  for (int r = tid; r < p.rows_pad; r += kConsumerWarps * 32) {
+  for (int r = tid; r < p.rows_pad; r += NTHR) {
     float M = -INFINITY;
     for (int c = c_first; c <= c_last; ++c) {
       bool used;
@@ -191,9 +191,9 @@ __device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t
     mlf[2 * r] = M;
     mlf[2 * r + 1] = den > 0.f ? p.v_scale / den : 0.f;
   }
-  named_barrier(1, kConsumerWarps * 32);
+  named_barrier(1, NTHR);
   const int64_t obase = static_cast<int64_t>(cur.b) * p.qo_len;
-  for (int e = tid; e < p.rows_pad * (D / 4); e += kConsumerWarps * 32) {
+  for (int e = tid; e < p.rows_pad * (D / 4); e += NTHR) {
     const int r = e / (D / 4), d = 4 * (e % (D / 4));
     const int t = r / p.group_pad, gl = r % p.group_pad;
     if (t >= p.qo_len || gl >= p.group) continue;

@@ -1,5 +1,6 @@
-// attn_bf16.cu -- instantiations of the attn kernel for bf16 KV caches.
+// attn_bf16.cu -- instantiations of the attention kernels (mma.sync and tcgen05) for bf16 KV caches.
 #include "attn.cuh"
+#include "attn_umma.cuh"
 #include "launch.h"
 
 namespace trtv {
@@ -32,6 +33,15 @@ cudaError_t launch_attn_bf16(int head_dim, int mt, const CUtensorMap& map, const
     }
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const AttnParams& p,
+                             int grid, size_t smem, cudaStream_t st) {
+  const void* fn = reinterpret_cast<const void*>(&attn_umma_kernel<128>);
+  cudaError_t e = ensure_smem_attr(fn, smem);
+  if (e != cudaSuccess) return e;
+  attn_umma_kernel<128><<<grid, kUmmaAttnThreads, smem, st>>>(kv_map, q_map, p);
+  return cudaGetLastError();
 }
 
 }  // namespace trtv

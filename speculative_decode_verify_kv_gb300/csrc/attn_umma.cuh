@@ -1,0 +1,423 @@
+// attn_umma.cuh -- ladder verify attention (dense and MSA sparse) on the
+// tcgen05 tensor cores, for bf16 K/V, head_dim 128, G = Hq / Hk a power of
+// two and G * qo_len <= 128 rows.
+//
+// Sources: "Eagle3 for M3 MSA path + CUDA graphs compatibility" (fork PR #3),
+// commit "... verify" (token t attends kv_len - qo_len + t + 1 positions; the
+// sparse pass attends the selected blocks); "Default Minimax-m3 to unified
+// draft-target kv manager" (#17835), "Grouped-HND draft KV transfer" (page
+// layout); "wrap up eagle changes in m3 side branch" (#18066), view commit
+// (K page at slot * stride, V page at slot * stride + 1).
+//
+// Work split as in attn_kernel (stream-K over the pages / selected blocks of
+// every (request, KV head) sequence, in-kernel merge of cut sequences).  Per
+// sequence the (token, group head) rows (row = t * G + g) are the M = 128
+// UMMA tile; per page:
+//   S = Q K^T       8 UMMA 128x128x16 -> TMEM S[buf] (fp32, lane = row)
+//   softmax         warps 0-3: tcgen05.ld of a row's 128 scores, mask, online
+//                   maximum in the log2 domain (O rescaled only when a row's
+//                   maximum rises by more than 8, the stale maximum is exact
+//                   since the final division uses the same one), P = 2^(x - m)
+//                   as bf16 pairs stored back over S[buf] columns 0..63
+//   O += P V        16 UMMA 128x64x16 with A = P in TMEM and B = the V page
+//                   (token rows, MN-major) -> TMEM O (fp32, 128 columns)
+// Warp 4 streams Q (3-D box per sequence) and the K and V pages (two rings of
+// 32 KB stages in the UMMA's 128B-swizzled layout); warp 5 lane 0 issues the
+// UMMAs, QK of page i + 1 ahead of PV of page i so the tensor core overlaps
+// the softmax (the last PV of a sequence is not held back).  TMEM: S[0] cols 0-127, S[1] 128-255, O 256-383.
+#pragma once
+
+#include "attn.cuh"
+#include "umma.cuh"
+
+namespace trtv {
+
+constexpr int kUmmaAttnThreads = 192;
+constexpr uint32_t kAttnTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+__global__ void __launch_bounds__(kUmmaAttnThreads, 1)
+    attn_umma_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                     const __grid_constant__ AttnParams p) {
+  static_assert(D == 128, "tcgen05 attention handles head_dim 128");
+  constexpr int KV = kGroups * 2 * kBox;  // one page of K (or V) for one head: 32 KB
+  constexpr int QBUF = 128 * D * 2;
+  constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 128);
+  constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 64) | (1u << 16);  // B (V) MN-major
+  constexpr uint32_t TM_O = 256;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int NK = p.nstages, NV = p.nv;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  uint64_t* kempty = kfull + NK;   // QK finished reading the K stage
+  uint64_t* vfull = kempty + NK;
+  uint64_t* vempty = vfull + NV;   // PV finished reading the V stage
+  uint64_t* sfull = vempty + NV;   // [2] S written
+  uint64_t* pfull = sfull + 2;     // [2] P written over S (4 softmax warps)
+  uint64_t* pvdone = pfull + 2;    // [2] PV of the page in that buffer retired
+  uint64_t* qfull = pvdone + 2;    // [2]
+  uint64_t* qempty = qfull + 2;    // [2] last QK of the sequence retired
+  uint64_t* mdone = qempty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mdone + 1);
+  int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
+  float* ml = reinterpret_cast<float*>(smem + p.off_ml);  // merge flags + row stats
+  const bool sparse = p.sparse != 0;
+  const int Hk = p.num_kv_heads, T = p.qo_len, G = p.group;
+  const int nitems = sparse ? p.batch * Hk : p.batch;
+  int32_t* warp_tot = scan + nitems + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NK; ++i) { mbar_init(&kfull[i], 1); mbar_init(&kempty[i], 1); }
+    for (int i = 0; i < NV; ++i) { mbar_init(&vfull[i], 1); mbar_init(&vempty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&pfull[i], 4);
+      mbar_init(&pvdone[i], 1);
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+    }
+    mbar_init(mdone, 1);
+    fence_mbar_init();
+  }
+  block_exclusive_scan(nitems, scan, warp_tot, [&](int i) -> int32_t {
+    if (sparse) return p.plan_count[i];
+    const int L = p.kv_lens[i];
+    if (len_valid(L, T, p.max_pages)) return (L + kPage - 1) / kPage;
+    if (blockIdx.x == 0) atomicOr(p.err, TRTV_DEVERR_KV_LEN);
+    return 0;
+  });
+  const int64_t W = item_start(scan, nitems, Hk, sparse);
+  for (int i = blockIdx.x; i < nitems; i += gridDim.x) {  // zero rows of empty sequences
+    if (scan[i + 1] != scan[i]) continue;
+    const int b = sparse ? i / Hk : i;
+    const int h0 = sparse ? i % Hk : 0, nh = sparse ? 1 : Hk;
+    const int span = nh * G * D;
+    for (int t = 0; t < T; ++t) {
+      const int64_t o0 = ((static_cast<int64_t>(b) * T + t) * p.num_q_heads + static_cast<int64_t>(h0) * G) * D;
+      for (int e = threadIdx.x; e < span; e += blockDim.x) {
+        if (p.out_f32) static_cast<float*>(p.out)[o0 + e] = 0.f;
+        else static_cast<__nv_bfloat16*>(p.out)[o0 + e] = __float2bfloat16(0.f);
+      }
+    }
+  }
+  if (W == 0) return;
+  const int64_t u0 = cta_unit_begin(blockIdx.x, W, p.num_ctas);
+  const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);
+  if (u0 >= u1) return;
+
+  if (warp == 5) {
+    tmem_alloc(tslot, kAttnTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  uint8_t* qbase = smem + p.off_q;
+  uint8_t* kring = smem + p.off_stage;
+  uint8_t* vring = smem + p.off_vring;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&kv_map);
+      prefetch_tensormap(&q_map);
+      const uint64_t pol = policy_evict_first();
+      const int sub_rows = Hk * kSub;
+      const uint32_t qbytes = static_cast<uint32_t>(2 * 64 * 2 * G * T);
+      int it = 0, sq = 0;
+      bool alive = true;
+      for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+           alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+           cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
+        const int qb = sq & 1;
+        if (sq >= 2 && !mbar_wait(&qempty[qb], static_cast<uint32_t>((sq >> 1) - 1) & 1u, p.err)) {
+          alive = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&qfull[qb], qbytes);
+        for (int hb = 0; hb < 2; ++hb)
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(qbase + qb * QBUF + hb * (QBUF / 2))),
+              "l"(reinterpret_cast<uint64_t>(&q_map)), "r"(hb * 64), "r"(cur.h * G), "r"(cur.b * T),
+              "r"(smem_u32(&qfull[qb]))
+              : "memory");
+        const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
+        const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+        for (int64_t j = j0; j < j1; ++j, ++it) {
+          const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
+                                 : static_cast<int>(j);
+          int slot = p.page_table[static_cast<int64_t>(cur.b) * p.max_pages + blk];
+          if (slot < 0 || slot >= p.num_slots) {
+            atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
+            slot = 0;
+          }
+          const int64_t kbuf = static_cast<int64_t>(slot) * p.slot_stride;
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const int n = kv ? NV : NK, st = it % n;
+            uint64_t* fb = kv ? &vfull[st] : &kfull[st];
+            uint64_t* eb = kv ? &vempty[st] : &kempty[st];
+            if (it >= n && !mbar_wait(eb, static_cast<uint32_t>(it / n - 1) & 1u, p.err)) {
+              alive = false;
+              break;
+            }
+            uint8_t* dst = (kv ? vring : kring) + st * KV;
+            mbar_arrive_expect_tx(fb, KV);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+              for (int g = 0; g < kGroups; ++g) {
+                const int y = static_cast<int>(((kbuf + kv) * kGroups + g) * sub_rows + cur.h * kSub);
+                tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, fb, hb * 64, y, pol);
+              }
+          }
+          if (!alive) break;
+        }
+      }
+      // never leave copies in flight
+      for (int k = (it > NK ? it - NK : 0); k < it; ++k)
+        mbar_wait(&kfull[k % NK], static_cast<uint32_t>(k / NK) & 1u, p.err);
+      for (int k = (it > NV ? it - NV : 0); k < it; ++k)
+        mbar_wait(&vfull[k % NV], static_cast<uint32_t>(k / NV) & 1u, p.err);
+      if (sq >= 1) mbar_wait(&qfull[(sq - 1) & 1], static_cast<uint32_t>((sq - 1) >> 1) & 1u, p.err);
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------- UMMA issuer
+    if (lane == 0) {
+      bool alive = true;
+      auto issue_pv = [&](int pg, bool first) {
+        const int vs = pg % NV, b = pg & 1;
+        if (!alive) return;
+        if (!mbar_wait(&vfull[vs], static_cast<uint32_t>(pg / NV) & 1u, p.err) ||
+            !mbar_wait(&pfull[b], static_cast<uint32_t>(pg >> 1) & 1u, p.err)) {
+          alive = false;
+          return;
+        }
+        tc_fence_after();
+        const uint32_t v0 = smem_u32(vring + vs * KV);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+            umma_bf16_tmem_a(tmem + TM_O + hb * 64, tmem + b * 128 + kk * 8,
+                             umma_desc_sw128_mn(v0 + hb * (KV / 2) + kk * 2048), IDESC_PV,
+                             (!first || kk > 0) ? 1u : 0u);
+        umma_commit(&vempty[vs]);
+        umma_commit(&pvdone[b]);
+      };
+      int it = 0, sq = 0, pend = -1;
+      bool pend_first = false;
+      for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+           alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+           cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
+        const int qb = sq & 1;
+        if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq >> 1) & 1u, p.err)) { alive = false; break; }
+        const uint32_t a0 = smem_u32(qbase + qb * QBUF);
+        const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
+        const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+        for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
+          const int ks = it % NK, buf = it & 1;
+          if (!mbar_wait(&kfull[ks], static_cast<uint32_t>(it / NK) & 1u, p.err) ||
+              (it >= 2 && !mbar_wait(&pvdone[buf], static_cast<uint32_t>((it >> 1) - 1) & 1u, p.err))) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k0 = smem_u32(kring + ks * KV);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            umma_bf16(tmem + buf * 128, umma_desc_sw128(a0 + (k >> 2) * (QBUF / 2) + (k & 3) * 32),
+                      umma_desc_sw128(k0 + (k >> 2) * (KV / 2) + (k & 3) * 32), IDESC_QK, k > 0);
+          umma_commit(&kempty[ks]);
+          umma_commit(&sfull[buf]);
+          if (j == j1 - 1) umma_commit(&qempty[qb]);
+          if (pend >= 0) issue_pv(pend, pend_first);
+          pend = it;
+          pend_first = j == j0;
+        }
+        // the sequence's last PV goes out now: its epilogue must not wait for
+        // the next sequence's Q tile and first QK
+        if (pend >= 0) issue_pv(pend, pend_first);
+        pend = -1;
+      }
+      umma_commit(mdone);
+      mbar_wait(mdone, 0, p.err);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------- softmax and epilogue
+    const int q = warp;  // TMEM lane quadrant
+    const int r = 32 * q + lane;
+    const int t = r / G, gl = r % G;
+    const bool valid = t < T;
+    const bool live = 32 * q < G * T;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    bool dead = false;
+    int it = 0;
+    for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+         (sparse ? cur.s : cur.b) < nitems && cur.start < u1; cursor_next(cur, scan, nitems, Hk, sparse)) {
+      const int L = p.kv_lens[cur.b];
+      const int bound = valid ? L - T + t : -1;
+      const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
+      const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+      float m_use = -INFINITY, l = 0.f;
+      for (int64_t j = j0; j < j1; ++j, ++it) {
+        const int buf = it & 1;
+        if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it >> 1) & 1u, p.err));
+        tc_fence_after();
+        if (live) {
+          int blk = static_cast<int>(j);
+          uint32_t tokmask = 0xffffffffu;
+          if (sparse) {
+            blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+            tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+          }
+          const int pos0 = blk * kPage;
+          const int bnd = (valid && ((tokmask >> t) & 1u)) ? bound : -1;
+          const bool masked = sparse || pos0 + kPage - 1 > L - T;
+          float x[128];
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            float v[32];
+            tmem_ld32(tl + buf * 128 + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[c0 + i] = v[i];
+          }
+          float mloc = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            float v = x[i] * p.scale_log2;
+            if (masked && pos0 + i > bnd) v = -INFINITY;
+            x[i] = v;
+            mloc = fmaxf(mloc, v);
+          }
+          const float m_new = fmaxf(m_use, mloc);
+          const bool need = m_use != -INFINITY && m_new > m_use + kRescaleLog2;
+          if (m_use == -INFINITY) m_use = m_new;
+          if (__any_sync(0xffffffffu, need)) {
+            // O must be stable: PV of the previous page has retired
+            if (!dead)
+              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[(it - 1) & 1],
+                                                        static_cast<uint32_t>((it - 1) >> 1) & 1u, p.err));
+            tc_fence_after();
+            const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
+            if (need) {
+              l *= alpha;
+              m_use = m_new;
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+              float v[32];
+              tmem_ld32(tl + TM_O + c0, v);
+              uint32_t w[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * alpha);
+              tmem_st32(tl + TM_O + c0, w);
+            }
+            tmem_st_wait();
+          }
+          const bool none = m_use == -INFINITY;
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float p0 = none ? 0.f : fast_exp2(x[2 * (c0 + i)] - m_use);
+              const float p1 = none ? 0.f : fast_exp2(x[2 * (c0 + i) + 1] - m_use);
+              l += p0 + p1;
+              __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+              w[i] = *reinterpret_cast<uint32_t*>(&pk);
+            }
+            tmem_st32(tl + buf * 128 + c0, w);
+          }
+          tmem_st_wait();
+        }
+        // V rows at or past kv_len may hold anything (NaN included): P is zero
+        // there, but 0 * NaN is not, so warp 0 zeroes them before PV reads V.
+        {
+          const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
+                                 : static_cast<int>(j);
+          const int nvalid = L - blk * kPage;
+          if (warp == 0 && nvalid < kPage) {
+            const int vs = it % NV;
+            if (!dead)
+              dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, p.err));
+            uint8_t* vst = vring + vs * KV;
+            const int nchunks = (kPage - nvalid) * 16;  // 2 column blocks x 8 chunks per token
+            for (int idx = lane; idx < nchunks; idx += 32) {
+              const int tok = nvalid + idx / 16, part = idx % 16;
+              *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
+                                        (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[buf]);
+      }
+      // ------------------------------------------------------- sequence end
+      const int last = it - 1;
+      if (!dead)
+        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last & 1], static_cast<uint32_t>(last >> 1) & 1u, p.err));
+      tc_fence_after();
+      const bool whole = u0 <= cur.start && cur.start + cur.units <= u1;
+      const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (cur.start <= u0 ? 0 : 1);
+      if (live) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float sc = whole ? inv * p.v_scale : inv;
+        const int64_t orow = ((static_cast<int64_t>(cur.b) * T + t) * p.num_q_heads +
+                              static_cast<int64_t>(cur.h) * G + gl) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          float v[32];
+          tmem_ld32(tl + TM_O + c0, v);
+          if (!valid) continue;
+          if (whole) {
+            if (p.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(v[4 * i] * sc, v[4 * i + 1] * sc, v[4 * i + 2] * sc, v[4 * i + 3] * sc);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  __nv_bfloat162 pk = __floats2bfloat162_rn(v[8 * i + 2 * k] * sc, v[8 * i + 2 * k + 1] * sc);
+                  w[k] = *reinterpret_cast<uint32_t*>(&pk);
+                }
+                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * p.rows_pad + r) * D + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(v[4 * i] * sc, v[4 * i + 1] * sc, v[4 * i + 2] * sc, v[4 * i + 3] * sc);
+          }
+        }
+        if (!whole && valid) p.ws_lse[slot * p.rows_pad + r] = l > 0.f ? m_use + __log2f(l) : -INFINITY;
+      }
+      tc_fence_before();
+      if (!whole) merge_if_last<D, 128>(p, cur, W, ml + 256, reinterpret_cast<int*>(ml));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kAttnTmemCols);
+  }
+}
+
+}  // namespace trtv

@@ -46,6 +46,7 @@ struct AttnParams {
   float v_scale;
   // dynamic shared memory carve-up (byte offsets from the 1024-aligned base)
   int off_stage, stage_bytes, off_k, off_v, off_conv, off_merge, off_ml, off_scan, off_bar;
+  int off_q, off_vring, nv;  // tcgen05 kernel: Q tiles, V ring (K ring at off_stage, nstages)
 };
 
 struct ProxyParams {

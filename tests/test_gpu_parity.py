@@ -169,9 +169,10 @@ def test_dense_edge_lengths():
     check_dense(p, num_ctas=11, out_dtype="f32")
 
 
-def test_dense_invalid_requests_are_zero_and_flagged():
+@pytest.mark.parametrize("D", [64, 128])
+def test_dense_invalid_requests_are_zero_and_flagged(D):
     p = W.make_problem(kv_lens=[300, 200, 100], qo_len=4, num_q_heads=8, num_kv_heads=2,
-                       head_dim=64, seed=4, max_pages_per_req=3)
+                       head_dim=D, seed=4, max_pages_per_req=3)
     lens = p.kv_lens.clone()
     lens[1] = 2           # shorter than qo_len
     lens[2] = 1000        # beyond capacity (3 pages)
@@ -181,6 +182,7 @@ def test_dense_invalid_requests_are_zero_and_flagged():
     err = T.trtv_get_device_error()
     assert err & T.DEVERR_KV_LEN
     assert torch.all(out[4:12] == 0)
+    out = out.reshape(12, 8, D)
     ref, bad = oracle.verify_dense(oracle.Inputs(p, kv_lens=lens))
     assert bad == 2
     assert np.abs(out.numpy() - ref).max() <= TOL_BF16
