@@ -222,14 +222,17 @@ bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
 }
 
 bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
-  const size_t qbufs = 2 * 128 * 128 * 2;
+  const size_t qbuf = 128 * 128 * 2;
   const size_t kv = static_cast<size_t>(kGroups) * 2 * kBox;
   const int nitems = sparse ? pl.n_seq : g->batch;
   const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
   const size_t ml = 512 * sizeof(float);
-  const int nk = 2, nv = 2;
-  size_t off = qbufs;
+  // one Q tile, two K stages, three V stages: V stages are held longest (until
+  // PV retires), so they get the depth
+  const int nq = kUmmaAttnQTiles, nk = kUmmaAttnKStages, nv = kUmmaAttnVStages;
+  size_t off = 0;
   a->off_q = 0;
+  off += nq * qbuf;
   a->off_stage = static_cast<int>(off);
   a->stage_bytes = static_cast<int>(kv);
   off += nk * kv;
@@ -243,6 +246,7 @@ bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnPa
   off = a->off_bar + (2 * nk + 2 * nv + 11) * sizeof(uint64_t) + 16;
   a->nstages = nk;
   a->nv = nv;
+  a->nq = nq;
   a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
   *bytes = off + kAlignSlack;
   return *bytes <= kSmemOptin;

@@ -21,8 +21,9 @@
 //                   as bf16 pairs stored back over S[buf] columns 0..63
 //   O += P V        16 UMMA 128x64x16 with A = P in TMEM and B = the V page
 //                   (token rows, MN-major) -> TMEM O (fp32, 128 columns)
-// Warp 4 streams Q (3-D box per sequence) and the K and V pages (two rings of
-// 32 KB stages in the UMMA's 128B-swizzled layout); warp 5 lane 0 issues the
+// Warp 4 streams Q (3-D box per sequence) and the K pages, warp 6 the V pages
+// (two rings of 32 KB stages in the UMMA's 128B-swizzled layout, each stream
+// as far ahead as its own ring allows); warp 5 lane 0 issues the
 // UMMAs, QK of page i + 1 ahead of PV of page i so the tensor core overlaps
 // the softmax (the last PV of a sequence is not held back).  TMEM: S[0] cols 0-127, S[1] 128-255, O 256-383.
 #pragma once
@@ -32,7 +33,7 @@
 
 namespace trtv {
 
-constexpr int kUmmaAttnThreads = 192;
+constexpr int kUmmaAttnThreads = 224;  // softmax warps 0-3, K/Q TMA 4, UMMA 5, V TMA 6
 constexpr uint32_t kAttnTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int NK = p.nstages, NV = p.nv;
+  const int NK = p.nstages, NV = p.nv, NQ = p.nq;
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* kempty = kfull + NK;   // QK finished reading the K stage
   uint64_t* vfull = kempty + NK;
@@ -121,32 +122,41 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint8_t* kring = smem + p.off_stage;
   uint8_t* vring = smem + p.off_vring;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------- TMA producers: K (+Q) and V
+    // Two independent streams: K pages are freed early (after QK), V pages
+    // late (after PV); one stream must not hold the other back.
     if (lane == 0) {
+      const bool is_v = warp == 6;
       prefetch_tensormap(&kv_map);
-      prefetch_tensormap(&q_map);
+      if (!is_v) prefetch_tensormap(&q_map);
       const uint64_t pol = policy_evict_first();
       const int sub_rows = Hk * kSub;
       const uint32_t qbytes = static_cast<uint32_t>(2 * 64 * 2 * G * T);
+      const int n = is_v ? NV : NK;
+      uint64_t* fullb = is_v ? vfull : kfull;
+      uint64_t* emptyb = is_v ? vempty : kempty;
+      uint8_t* ring = is_v ? vring : kring;
       int it = 0, sq = 0;
       bool alive = true;
       for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
            alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
-        const int qb = sq & 1;
-        if (sq >= 2 && !mbar_wait(&qempty[qb], static_cast<uint32_t>((sq >> 1) - 1) & 1u, p.err)) {
-          alive = false;
-          break;
+        if (!is_v) {
+          const int qb = sq % NQ;
+          if (sq >= NQ && !mbar_wait(&qempty[qb], static_cast<uint32_t>(sq / NQ - 1) & 1u, p.err)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&qfull[qb], qbytes);
+          for (int hb = 0; hb < 2; ++hb)
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(qbase + qb * QBUF + hb * (QBUF / 2))),
+                "l"(reinterpret_cast<uint64_t>(&q_map)), "r"(hb * 64), "r"(cur.h * G), "r"(cur.b * T),
+                "r"(smem_u32(&qfull[qb]))
+                : "memory");
         }
-        mbar_arrive_expect_tx(&qfull[qb], qbytes);
-        for (int hb = 0; hb < 2; ++hb)
-          asm volatile(
-              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(qbase + qb * QBUF + hb * (QBUF / 2))),
-              "l"(reinterpret_cast<uint64_t>(&q_map)), "r"(hb * 64), "r"(cur.h * G), "r"(cur.b * T),
-              "r"(smem_u32(&qfull[qb]))
-              : "memory");
         const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
         const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
         for (int64_t j = j0; j < j1; ++j, ++it) {
@@ -154,38 +164,31 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
                                  : static_cast<int>(j);
           int slot = p.page_table[static_cast<int64_t>(cur.b) * p.max_pages + blk];
           if (slot < 0 || slot >= p.num_slots) {
-            atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
+            if (!is_v) atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
             slot = 0;
           }
-          const int64_t kbuf = static_cast<int64_t>(slot) * p.slot_stride;
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            const int n = kv ? NV : NK, st = it % n;
-            uint64_t* fb = kv ? &vfull[st] : &kfull[st];
-            uint64_t* eb = kv ? &vempty[st] : &kempty[st];
-            if (it >= n && !mbar_wait(eb, static_cast<uint32_t>(it / n - 1) & 1u, p.err)) {
-              alive = false;
-              break;
-            }
-            uint8_t* dst = (kv ? vring : kring) + st * KV;
-            mbar_arrive_expect_tx(fb, KV);
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-              for (int g = 0; g < kGroups; ++g) {
-                const int y = static_cast<int>(((kbuf + kv) * kGroups + g) * sub_rows + cur.h * kSub);
-                tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, fb, hb * 64, y, pol);
-              }
+          const int64_t buf = static_cast<int64_t>(slot) * p.slot_stride + (is_v ? 1 : 0);
+          const int st = it % n;
+          if (it >= n && !mbar_wait(&emptyb[st], static_cast<uint32_t>(it / n - 1) & 1u, p.err)) {
+            alive = false;
+            break;
           }
-          if (!alive) break;
+          uint8_t* dst = ring + st * KV;
+          mbar_arrive_expect_tx(&fullb[st], KV);
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) {
+              const int y = static_cast<int>((buf * kGroups + g) * sub_rows + cur.h * kSub);
+              tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, &fullb[st], hb * 64, y, pol);
+            }
         }
       }
       // never leave copies in flight
-      for (int k = (it > NK ? it - NK : 0); k < it; ++k)
-        mbar_wait(&kfull[k % NK], static_cast<uint32_t>(k / NK) & 1u, p.err);
-      for (int k = (it > NV ? it - NV : 0); k < it; ++k)
-        mbar_wait(&vfull[k % NV], static_cast<uint32_t>(k / NV) & 1u, p.err);
-      if (sq >= 1) mbar_wait(&qfull[(sq - 1) & 1], static_cast<uint32_t>((sq - 1) >> 1) & 1u, p.err);
+      for (int k = (it > n ? it - n : 0); k < it; ++k)
+        mbar_wait(&fullb[k % n], static_cast<uint32_t>(k / n) & 1u, p.err);
+      if (!is_v && sq >= 1)
+        mbar_wait(&qfull[(sq - 1) % NQ], static_cast<uint32_t>((sq - 1) / NQ) & 1u, p.err);
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------- UMMA issuer
@@ -216,8 +219,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
            alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
-        const int qb = sq & 1;
-        if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq >> 1) & 1u, p.err)) { alive = false; break; }
+        const int qb = sq % NQ;
+        if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err)) { alive = false; break; }
         const uint32_t a0 = smem_u32(qbase + qb * QBUF);
         const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
         const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
