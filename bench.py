@@ -378,7 +378,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="dense", choices=["dense", "msa", "fp8", "long"])
-    ap.add_argument("--paths", default="msa", help="extra workloads timed alongside (comma list)")
+    ap.add_argument("--paths", default="msa,fp8,long",
+                    help="extra workloads timed alongside (comma list, or none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
@@ -437,7 +438,7 @@ def main():
 
     paths = {}
     for extra in [w for w in args.paths.split(",") if w and w not in (args.workload, "none")]:
-        r = time_path(extra, max(10, args.steps // 4), args.warmup)
+        r = time_path(extra, max(10, args.steps // 8), args.warmup)
         pe = r["p"]
         per = {}
         for n, b in r["bytes"].items():
@@ -453,6 +454,7 @@ def main():
             pv["unique_blocks_mean"] = r["unique_blocks_mean"]
         paths[extra] = pv
         del r
+        _CACHE.pop(extra, None)
         torch.cuda.empty_cache()
 
     e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)

@@ -226,7 +226,7 @@ bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnPa
   const size_t kv = static_cast<size_t>(kGroups) * 2 * kBox;
   const int nitems = sparse ? pl.n_seq : g->batch;
   const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
-  const size_t ml = 512 * sizeof(float);
+  const size_t ml = 1280 * sizeof(float);
   // one Q tile, two K stages, three V stages: V stages are held longest (until
   // PV retires), so they get the depth
   const int nq = kUmmaAttnQTiles, nk = kUmmaAttnKStages, nv = kUmmaAttnVStages;
@@ -243,7 +243,7 @@ bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnPa
   a->off_ml = static_cast<int>(off);
   off += ml;
   a->off_bar = static_cast<int>(align_up(off, 8));
-  off = a->off_bar + (2 * nk + 2 * nv + 11) * sizeof(uint64_t) + 16;
+  off = a->off_bar + (2 * nk + 2 * nv + 16) * sizeof(uint64_t) + 16;
   a->nstages = nk;
   a->nv = nv;
   a->nq = nq;

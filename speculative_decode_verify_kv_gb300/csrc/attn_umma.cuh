@@ -14,18 +14,21 @@
 // sequence the (token, group head) rows (row = t * G + g) are the M = 128
 // UMMA tile; per page:
 //   S = Q K^T       8 UMMA 128x128x16 -> TMEM S[buf] (fp32, lane = row)
-//   softmax         warps 0-3: tcgen05.ld of a row's 128 scores, mask, online
-//                   maximum in the log2 domain (O rescaled only when a row's
-//                   maximum rises by more than 8, the stale maximum is exact
-//                   since the final division uses the same one), P = 2^(x - m)
-//                   as bf16 pairs stored back over S[buf] columns 0..63
+//   softmax         warps 0-7: warp w reads TMEM lane quadrant w % 4 and
+//                   columns 64 (w / 4) .. + 63 of each row; the two warps of a
+//                   quadrant swap their row maxima through shared memory.
+//                   Online maximum in the log2 domain (O rescaled only when a
+//                   row's maximum rises by more than 8; the stale maximum is
+//                   exact since the final division uses the same one),
+//                   P = 2^(x - m) as bf16 pairs stored back over S[buf]
 //   O += P V        16 UMMA 128x64x16 with A = P in TMEM and B = the V page
 //                   (token rows, MN-major) -> TMEM O (fp32, 128 columns)
-// Warp 4 streams Q (3-D box per sequence) and the K pages, warp 6 the V pages
+// Warp 8 streams Q (3-D box per sequence) and the K pages, warp 10 the V pages
 // (two rings of 32 KB stages in the UMMA's 128B-swizzled layout, each stream
-// as far ahead as its own ring allows); warp 5 lane 0 issues the
+// as far ahead as its own ring allows); warp 9 lane 0 issues the
 // UMMAs, QK of page i + 1 ahead of PV of page i so the tensor core overlaps
-// the softmax (the last PV of a sequence is not held back).  TMEM: S[0] cols 0-127, S[1] 128-255, O 256-383.
+// the softmax (the last PV of a sequence is not held back).  TMEM: three S
+// buffers at columns 0, 128, 256 and O at 384.
 #pragma once
 
 #include "attn.cuh"
@@ -33,7 +36,8 @@
 
 namespace trtv {
 
-constexpr int kUmmaAttnThreads = 224;  // softmax warps 0-3, K/Q TMA 4, UMMA 5, V TMA 6
+constexpr int kUmmaAttnThreads = 352;  // softmax warps 0-7, K/Q TMA 8, UMMA 9, V TMA 10
+constexpr int kSBufs = 3;
 constexpr uint32_t kAttnTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -46,7 +50,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   constexpr int QBUF = 128 * D * 2;
   constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 128);
   constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 64) | (1u << 16);  // B (V) MN-major
-  constexpr uint32_t TM_O = 256;
+  constexpr uint32_t TM_O = 384;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -56,15 +60,17 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint64_t* kempty = kfull + NK;   // QK finished reading the K stage
   uint64_t* vfull = kempty + NK;
   uint64_t* vempty = vfull + NV;   // PV finished reading the V stage
-  uint64_t* sfull = vempty + NV;   // [2] S written
-  uint64_t* pfull = sfull + 2;     // [2] P written over S (4 softmax warps)
-  uint64_t* pvdone = pfull + 2;    // [2] PV of the page in that buffer retired
-  uint64_t* qfull = pvdone + 2;    // [2]
+  uint64_t* sfull = vempty + NV;        // [3] S written
+  uint64_t* pfull = sfull + kSBufs;     // [3] P written over S (8 softmax warps)
+  uint64_t* pvdone = pfull + kSBufs;    // [3] PV of the page in that buffer retired
+  uint64_t* qfull = pvdone + kSBufs;    // [2]
   uint64_t* qempty = qfull + 2;    // [2] last QK of the sequence retired
   uint64_t* mdone = qempty + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mdone + 1);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
-  float* ml = reinterpret_cast<float*>(smem + p.off_ml);  // merge flags + row stats
+  // [0,256) merge flags, [256,512) merge row stats, [512,1024) row maxima of
+  // the two column halves (double-buffered by page), [1024,1280) row sums
+  float* ml = reinterpret_cast<float*>(smem + p.off_ml);
   const bool sparse = p.sparse != 0;
   const int Hk = p.num_kv_heads, T = p.qo_len, G = p.group;
   const int nitems = sparse ? p.batch * Hk : p.batch;
@@ -74,10 +80,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) { mbar_init(&kfull[i], 1); mbar_init(&kempty[i], 1); }
     for (int i = 0; i < NV; ++i) { mbar_init(&vfull[i], 1); mbar_init(&vempty[i], 1); }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&pfull[i], 4);
+      mbar_init(&pfull[i], 8);
       mbar_init(&pvdone[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
     }
@@ -110,7 +118,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);
   if (u0 >= u1) return;
 
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tslot, kAttnTmemCols);
     tmem_relinquish();
   }
@@ -122,12 +130,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint8_t* kring = smem + p.off_stage;
   uint8_t* vring = smem + p.off_vring;
 
-  if (warp == 4 || warp == 6) {
+  if (warp == 8 || warp == 10) {
     // ------------------------------------------- TMA producers: K (+Q) and V
     // Two independent streams: K pages are freed early (after QK), V pages
     // late (after PV); one stream must not hold the other back.
     if (lane == 0) {
-      const bool is_v = warp == 6;
+      const bool is_v = warp == 10;
       prefetch_tensormap(&kv_map);
       if (!is_v) prefetch_tensormap(&q_map);
       const uint64_t pol = policy_evict_first();
@@ -190,15 +198,15 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       if (!is_v && sq >= 1)
         mbar_wait(&qfull[(sq - 1) % NQ], static_cast<uint32_t>((sq - 1) / NQ) & 1u, p.err);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ----------------------------------------------------------- UMMA issuer
     if (lane == 0) {
       bool alive = true;
       auto issue_pv = [&](int pg, bool first) {
-        const int vs = pg % NV, b = pg & 1;
+        const int vs = pg % NV, b = pg % kSBufs;
         if (!alive) return;
         if (!mbar_wait(&vfull[vs], static_cast<uint32_t>(pg / NV) & 1u, p.err) ||
-            !mbar_wait(&pfull[b], static_cast<uint32_t>(pg >> 1) & 1u, p.err)) {
+            !mbar_wait(&pfull[b], static_cast<uint32_t>(pg / kSBufs) & 1u, p.err)) {
           alive = false;
           return;
         }
@@ -225,9 +233,9 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
         const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
         for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
-          const int ks = it % NK, buf = it & 1;
+          const int ks = it % NK, buf = it % kSBufs;
           if (!mbar_wait(&kfull[ks], static_cast<uint32_t>(it / NK) & 1u, p.err) ||
-              (it >= 2 && !mbar_wait(&pvdone[buf], static_cast<uint32_t>((it >> 1) - 1) & 1u, p.err))) {
+              (it >= kSBufs && !mbar_wait(&pvdone[buf], static_cast<uint32_t>(it / kSBufs - 1) & 1u, p.err))) {
             alive = false;
             break;
           }
@@ -255,12 +263,15 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     __syncwarp();
   } else {
     // -------------------------------------------------- softmax and epilogue
-    const int q = warp;  // TMEM lane quadrant
+    const int q = warp & 3;            // TMEM lane quadrant
+    const int hf = warp >> 2;          // column half of every row
     const int r = 32 * q + lane;
     const int t = r / G, gl = r % G;
     const bool valid = t < T;
-    const bool live = 32 * q < G * T;
+    const bool live = 32 * q < G * T;  // same for both warps of a quadrant
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    float* xmax = ml + 512;            // [2 pages][2 halves][128 rows]
+    float* xl = ml + 1024;             // [2 halves][128 rows]
     bool dead = false;
     int it = 0;
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
@@ -271,43 +282,45 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
       float m_use = -INFINITY, l = 0.f;
       for (int64_t j = j0; j < j1; ++j, ++it) {
-        const int buf = it & 1;
-        if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it >> 1) & 1u, p.err));
+        const int buf = it % kSBufs;
+        if (!dead)
+          dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, p.err));
         tc_fence_after();
+        int blk = static_cast<int>(j);
+        uint32_t tokmask = 0xffffffffu;
+        if (sparse) {
+          blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+          tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+        }
+        const int pos0 = blk * kPage;
         if (live) {
-          int blk = static_cast<int>(j);
-          uint32_t tokmask = 0xffffffffu;
-          if (sparse) {
-            blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
-            tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
-          }
-          const int pos0 = blk * kPage;
           const int bnd = (valid && ((tokmask >> t) & 1u)) ? bound : -1;
           const bool masked = sparse || pos0 + kPage - 1 > L - T;
-          float x[128];
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            float v[32];
-            tmem_ld32(tl + buf * 128 + c0, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[c0 + i] = v[i];
-          }
+          uint32_t ra[32], rb[32];
+          tmem_ld32_async(tl + buf * 128 + hf * 64, ra);
+          tmem_ld32_async(tl + buf * 128 + hf * 64 + 32, rb);
+          tmem_ld_wait_dep(ra);
+          tmem_ld_wait_dep(rb);
+          float x[64];
           float mloc = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            float v = x[i] * p.scale_log2;
-            if (masked && pos0 + i > bnd) v = -INFINITY;
+          for (int i = 0; i < 64; ++i) {
+            float v = __uint_as_float(i < 32 ? ra[i] : rb[i - 32]) * p.scale_log2;
+            if (masked && pos0 + hf * 64 + i > bnd) v = -INFINITY;
             x[i] = v;
             mloc = fmaxf(mloc, v);
           }
+          xmax[((it & 1) * 2 + hf) * 128 + r] = mloc;
+          named_barrier(2 + q, 64);
+          mloc = fmaxf(mloc, xmax[((it & 1) * 2 + (hf ^ 1)) * 128 + r]);
           const float m_new = fmaxf(m_use, mloc);
           const bool need = m_use != -INFINITY && m_new > m_use + kRescaleLog2;
           if (m_use == -INFINITY) m_use = m_new;
           if (__any_sync(0xffffffffu, need)) {
             // O must be stable: PV of the previous page has retired
+            const int pv = it - 1;
             if (!dead)
-              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[(it - 1) & 1],
-                                                        static_cast<uint32_t>((it - 1) >> 1) & 1u, p.err));
+              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[pv % kSBufs], static_cast<uint32_t>(pv / kSBufs) & 1u, p.err));
             tc_fence_after();
             const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
             if (need) {
@@ -315,51 +328,44 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
               m_use = m_new;
             }
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-              float v[32];
-              tmem_ld32(tl + TM_O + c0, v);
+            for (int c0 = 0; c0 < 64; c0 += 32) {
               uint32_t w[32];
+              tmem_ld32_async(tl + TM_O + hf * 64 + c0, w);
+              tmem_ld_wait_dep(w);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * alpha);
-              tmem_st32(tl + TM_O + c0, w);
+              for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+              tmem_st32(tl + TM_O + hf * 64 + c0, w);
             }
             tmem_st_wait();
           }
           const bool none = m_use == -INFINITY;
+          uint32_t w[32];
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float p0 = none ? 0.f : fast_exp2(x[2 * (c0 + i)] - m_use);
-              const float p1 = none ? 0.f : fast_exp2(x[2 * (c0 + i) + 1] - m_use);
-              l += p0 + p1;
-              __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-              w[i] = *reinterpret_cast<uint32_t*>(&pk);
-            }
-            tmem_st32(tl + buf * 128 + c0, w);
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = none ? 0.f : fast_exp2(x[2 * i] - m_use);
+            const float p1 = none ? 0.f : fast_exp2(x[2 * i + 1] - m_use);
+            l += p0 + p1;
+            __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+            w[i] = *reinterpret_cast<uint32_t*>(&pk);
           }
+          tmem_st32(tl + buf * 128 + hf * 32, w);
           tmem_st_wait();
         }
         // V rows at or past kv_len may hold anything (NaN included): P is zero
         // there, but 0 * NaN is not, so warp 0 zeroes them before PV reads V.
-        {
-          const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
-                                 : static_cast<int>(j);
-          const int nvalid = L - blk * kPage;
-          if (warp == 0 && nvalid < kPage) {
-            const int vs = it % NV;
-            if (!dead)
-              dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, p.err));
-            uint8_t* vst = vring + vs * KV;
-            const int nchunks = (kPage - nvalid) * 16;  // 2 column blocks x 8 chunks per token
-            for (int idx = lane; idx < nchunks; idx += 32) {
-              const int tok = nvalid + idx / 16, part = idx % 16;
-              *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
-                                        (part & 7) * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
+        const int nvalid = L - pos0;
+        if (warp == 0 && nvalid < kPage) {
+          const int vs = it % NV;
+          if (!dead)
+            dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, p.err));
+          uint8_t* vst = vring + vs * KV;
+          const int nchunks = (kPage - nvalid) * 16;  // 2 column blocks x 8 chunks per token
+          for (int idx = lane; idx < nchunks; idx += 32) {
+            const int tok = nvalid + idx / 16, part = idx % 16;
+            *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
+                                      (part & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
         tc_fence_before();
         __syncwarp();
@@ -368,56 +374,67 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       // ------------------------------------------------------- sequence end
       const int last = it - 1;
       if (!dead)
-        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last & 1], static_cast<uint32_t>(last >> 1) & 1u, p.err));
+        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last % kSBufs], static_cast<uint32_t>(last / kSBufs) & 1u, p.err));
       tc_fence_after();
       const bool whole = u0 <= cur.start && cur.start + cur.units <= u1;
       const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (cur.start <= u0 ? 0 : 1);
       if (live) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        xl[hf * 128 + r] = l;
+        named_barrier(2 + q, 64);
+        const float lt = l + xl[(hf ^ 1) * 128 + r];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
         const float sc = whole ? inv * p.v_scale : inv;
         const int64_t orow = ((static_cast<int64_t>(cur.b) * T + t) * p.num_q_heads +
-                              static_cast<int64_t>(cur.h) * G + gl) * D;
+                              static_cast<int64_t>(cur.h) * G + gl) * D + hf * 64;
+        uint32_t oa[32], ob[32];
+        tmem_ld32_async(tl + TM_O + hf * 64, oa);
+        tmem_ld32_async(tl + TM_O + hf * 64 + 32, ob);
+        tmem_ld_wait_dep(oa);
+        tmem_ld_wait_dep(ob);
+        if (valid) {
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          float v[32];
-          tmem_ld32(tl + TM_O + c0, v);
-          if (!valid) continue;
-          if (whole) {
-            if (p.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c0);
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            const uint32_t* v = c0 ? ob : oa;
+            if (whole) {
+              if (p.out_f32) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  dst[i] = make_float4(__uint_as_float(v[4 * i]) * sc, __uint_as_float(v[4 * i + 1]) * sc,
+                                       __uint_as_float(v[4 * i + 2]) * sc, __uint_as_float(v[4 * i + 3]) * sc);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint32_t w4[4];
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * k]) * sc,
+                                                              __uint_as_float(v[8 * i + 2 * k + 1]) * sc);
+                    w4[k] = *reinterpret_cast<uint32_t*>(&pk);
+                  }
+                  dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * p.rows_pad + r) * D + hf * 64 + c0);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i] * sc, v[4 * i + 1] * sc, v[4 * i + 2] * sc, v[4 * i + 3] * sc);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + c0);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  __nv_bfloat162 pk = __floats2bfloat162_rn(v[8 * i + 2 * k] * sc, v[8 * i + 2 * k + 1] * sc);
-                  w[k] = *reinterpret_cast<uint32_t*>(&pk);
-                }
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
+                dst[i] = make_float4(__uint_as_float(v[4 * i]) * sc, __uint_as_float(v[4 * i + 1]) * sc,
+                                     __uint_as_float(v[4 * i + 2]) * sc, __uint_as_float(v[4 * i + 3]) * sc);
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * p.rows_pad + r) * D + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(v[4 * i] * sc, v[4 * i + 1] * sc, v[4 * i + 2] * sc, v[4 * i + 3] * sc);
           }
+          if (!whole && hf == 0) p.ws_lse[slot * p.rows_pad + r] = lt > 0.f ? m_use + __log2f(lt) : -INFINITY;
         }
-        if (!whole && valid) p.ws_lse[slot * p.rows_pad + r] = l > 0.f ? m_use + __log2f(l) : -INFINITY;
       }
       tc_fence_before();
-      if (!whole) merge_if_last<D, 128>(p, cur, W, ml + 256, reinterpret_cast<int*>(ml));
+      if (!whole) merge_if_last<D, 256>(p, cur, W, ml + 256, reinterpret_cast<int*>(ml));
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kAttnTmemCols);
   }
