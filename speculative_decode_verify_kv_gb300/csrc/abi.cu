@@ -215,10 +215,11 @@ bool encode_q_map(const trtv_geom* g, const Plan& pl, const void* q, CUtensorMap
 }
 
 // The tcgen05 attention kernel covers bf16, head_dim 128 and a power-of-two
-// group with group * qo_len <= 128 rows (one UMMA M = 128 tile).
+// group with 32 < group * qo_len <= 128 rows (one UMMA M = 128 tile).
+// Below 33 rows the mma.sync kernel keeps pace with the HBM stream and is used.
 bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
   return g->kv_dtype == TRTV_BF16 && g->head_dim == 128 && pl.group == pl.group_pad &&
-         pl.group * g->qo_len <= 128 && aligned(q, 16);
+         pl.group * g->qo_len > 32 && pl.group * g->qo_len <= 128 && aligned(q, 16);
 }
 
 bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {

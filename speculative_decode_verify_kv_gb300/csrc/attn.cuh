@@ -457,44 +457,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // ---- mask (ladder bound, selected tokens, kv_len) and online softmax
+        // ---- mask (ladder bound, selected tokens, kv_len) and online softmax.
+        // Chunks wholly below the lowest ladder bound need no mask (rows
+        // outside the tile see S = 0 from their zero Q and are never output).
+        // The reference maximum m_r of a row moves only when the row maximum
+        // grows past it by more than 8 (log2 units): P = 2^(x - m_r) stays
+        // below 2^8, the division by l uses the same m_r, and O is rescaled
+        // only on those rare moves.
+        const bool need_mask = sparse || pos0 + ct + CH - 1 > L - T;
         float mx[2] = {-INFINITY, -INFINITY};
+        if (need_mask) {
 #pragma unroll
-        for (int jt = 0; jt < NT; ++jt) {
+          for (int jt = 0; jt < NT; ++jt) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int pos = pos0 + ct + 8 * jt + 2 * c + (e & 1);
-            const float x = s[jt][e] * p.scale_log2;
-            s[jt][e] = (pos <= bnd[e >> 1]) ? x : -INFINITY;
-            mx[e >> 1] = fmaxf(mx[e >> 1], s[jt][e]);
+            for (int e = 0; e < 4; ++e) {
+              const int pos = pos0 + ct + 8 * jt + 2 * c + (e & 1);
+              const float x = s[jt][e] * p.scale_log2;
+              s[jt][e] = (pos <= bnd[e >> 1]) ? x : -INFINITY;
+              mx[e >> 1] = fmaxf(mx[e >> 1], s[jt][e]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int jt = 0; jt < NT; ++jt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              s[jt][e] *= p.scale_log2;
+              mx[e >> 1] = fmaxf(mx[e >> 1], s[jt][e]);
+            }
           }
         }
-        float alpha[2], muse[2];
+        float alpha[2];
+        bool grow[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
           mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
-          const float mn = fmaxf(m_r[hh], mx[hh]);
-          muse[hh] = (mn == -INFINITY) ? 0.f : mn;
-          alpha[hh] = fast_exp2(m_r[hh] - muse[hh]);
-          m_r[hh] = mn;
+          const float mc = fmaxf(m_r[hh], mx[hh]);
+          grow[hh] = (m_r[hh] == -INFINITY) ? (mc != -INFINITY) : (mc > m_r[hh] + 8.0f);
+          alpha[hh] = 1.f;
+          if (grow[hh]) {
+            alpha[hh] = (m_r[hh] == -INFINITY) ? 0.f : fast_exp2(m_r[hh] - mc);
+            m_r[hh] = mc;
+          }
         }
         float rs[2] = {0.f, 0.f};
 #pragma unroll
         for (int jt = 0; jt < NT; ++jt) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            s[jt][e] = fast_exp2(s[jt][e] - muse[e >> 1]);
+            const float mu = m_r[e >> 1];
+            s[jt][e] = (mu == -INFINITY) ? 0.f : fast_exp2(s[jt][e] - mu);
             rs[e >> 1] += s[jt][e];
           }
         }
-        l_r[0] = l_r[0] * alpha[0] + rs[0];
-        l_r[1] = l_r[1] * alpha[1] + rs[1];
+        if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
+          l_r[0] *= alpha[0];
+          l_r[1] *= alpha[1];
 #pragma unroll
-        for (int i = 0; i < DT; ++i) {
-          o[i][0] *= alpha[0]; o[i][1] *= alpha[0];
-          o[i][2] *= alpha[1]; o[i][3] *= alpha[1];
+          for (int i = 0; i < DT; ++i) {
+            o[i][0] *= alpha[0]; o[i][1] *= alpha[0];
+            o[i][2] *= alpha[1]; o[i][3] *= alpha[1];
+          }
         }
+        l_r[0] += rs[0];
+        l_r[1] += rs[1];
         // ---- O += P V
         const uint8_t* vb = vst + sp * SUBV;
         const bool tail = pos0 + ct + CH > L;   // rows past kv_len may hold anything

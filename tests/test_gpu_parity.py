@@ -123,10 +123,11 @@ def test_dense_qo_len_1_is_decode():
     check_dense(p, out_dtype="f32")
 
 
-def test_dense_stale_pages_hold_nan():
+@pytest.mark.parametrize("Hq,Hk", [(8, 2), (32, 2)])  # 16 rows (mma.sync), 64 rows (tcgen05)
+def test_dense_stale_pages_hold_nan(Hq, Hk):
     """Positions past kv_len inside a page and unused slots hold NaN: the
     output must not see them."""
-    p = W.make_problem(kv_lens=[100, 257, 130], qo_len=4, num_q_heads=8, num_kv_heads=2,
+    p = W.make_problem(kv_lens=[100, 257, 130], qo_len=4, num_q_heads=Hq, num_kv_heads=Hk,
                        head_dim=128, seed=9, slack_slots=3, fill_unused_with=float("nan"))
     pool = p.pool.clone()
     x = oracle.Inputs(p)
@@ -198,12 +199,13 @@ def test_dense_bad_page_id_flagged():
     assert T.trtv_get_device_error() & T.DEVERR_PAGE_ID
 
 
-def test_dense_graph_replay_with_mutated_lens():
+@pytest.mark.parametrize("Hq", [32, 64])  # 32 rows (mma.sync), 64 rows (tcgen05)
+def test_dense_graph_replay_with_mutated_lens(Hq):
     """Capture once, then grow and shrink kv_lens on the device between replays
     (including beyond the first call's maximum): every replay matches."""
-    p = W.make_problem(kv_lens=[200, 900, 50, 1400], qo_len=4, num_q_heads=32, num_kv_heads=4,
+    p = W.make_problem(kv_lens=[200, 900, 50, 1400], qo_len=4, num_q_heads=Hq, num_kv_heads=4,
                        head_dim=128, seed=8, max_pages_per_req=16, slack_slots=40)
-    full = W.make_problem(kv_lens=[2048, 2048, 2048, 2048], qo_len=4, num_q_heads=32, num_kv_heads=4,
+    full = W.make_problem(kv_lens=[2048, 2048, 2048, 2048], qo_len=4, num_q_heads=Hq, num_kv_heads=4,
                           head_dim=128, seed=8, max_pages_per_req=16)
     dv = DeviceVerify(full, out_dtype="f32")
     s = torch.cuda.Stream()
