@@ -149,6 +149,28 @@ trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* 
                               void* stream);
 
 /*
+ * trtv_verify_dense without a caller-provided workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory themselves -- for example a plugin whose host
+ * framework owns every device allocation and hands it no allocator, or code
+ * that must not call cudaMalloc between its setup and its steady state.
+ * Same arguments, results and errors as trtv_verify_dense, minus workspace.
+ * Scratch: one static 24 MiB device array per GPU that loads the library,
+ * held until the process exits.  A geometry whose trtv_workspace_bytes(geom,
+ * 0) exceeds 24 MiB is rejected with TRTV_ERR_WORKSPACE before anything is
+ * enqueued.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) -- make that first call before any stream capture.
+ * Every call enqueues a cudaMemsetAsync of the split counters and then the
+ * attention kernel; it allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).  All calls on a device share the one array:
+ * calls that may overlap on the GPU (different streams without ordering)
+ * race on it and must not be issued.
+ */
+trtv_status trtv_verify_dense_noalloc(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                      const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                      int32_t out_dtype, void* stream);
+
+/*
  * MSA proxy (OnlyScore) block scores (source: PR #3 "... verify" commit:
  * natively multi-token, inclusive causal bound with offset kv_len - qo_len).
  * scores[b][t][h][j] (fp32 [batch, qo_len, num_kv_heads, max_pages_per_req])

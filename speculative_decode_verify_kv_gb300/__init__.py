@@ -19,6 +19,7 @@ __all__ = [
     "TRTV_OK", "TRTV_BF16", "TRTV_FP8_E4M3", "TRTV_F32", "TrtvError", "Geom", "load",
     "trtv_subpage_view", "trtv_workspace_bytes", "trtv_verify_dense", "trtv_msa_proxy_score",
     "trtv_msa_topk", "trtv_msa_sparse_attn", "trtv_get_device_error", "trtv_version",
+    "trtv_verify_dense_noalloc",
     "trtv_status_string", "geom_of", "EXPORTS",
 ]
 
@@ -28,8 +29,8 @@ DEVERR_KV_LEN, DEVERR_PAGE_ID, DEVERR_BLOCK_IDX, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 # every function the C header declares
 EXPORTS = ("trtv_status_string", "trtv_version", "trtv_subpage_view", "trtv_workspace_bytes",
-           "trtv_verify_dense", "trtv_msa_proxy_score", "trtv_msa_topk", "trtv_msa_sparse_attn",
-           "trtv_get_device_error")
+           "trtv_verify_dense", "trtv_verify_dense_noalloc", "trtv_msa_proxy_score", "trtv_msa_topk",
+           "trtv_msa_sparse_attn", "trtv_get_device_error")
 
 
 class TrtvError(RuntimeError):
@@ -80,6 +81,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     h.trtv_workspace_bytes.argtypes = [G, i32]
     h.trtv_verify_dense.restype = ctypes.c_int
     h.trtv_verify_dense.argtypes = [G, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+    h.trtv_verify_dense_noalloc.restype = ctypes.c_int
+    h.trtv_verify_dense_noalloc.argtypes = [G, vp, vp, vp, vp, vp, i32, vp]
     h.trtv_msa_proxy_score.restype = ctypes.c_int
     h.trtv_msa_proxy_score.argtypes = [G, vp, vp, vp, vp, vp, vp]
     h.trtv_msa_topk.restype = ctypes.c_int
@@ -153,6 +156,15 @@ def trtv_verify_dense(geom: Geom, q, kv_pool, page_table, kv_lens, out, out_dtyp
     _check("trtv_verify_dense", load().trtv_verify_dense(
         ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens), _ptr(out),
         out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_verify_dense_noalloc(geom: Geom, q, kv_pool, page_table, kv_lens, out, out_dtype: int,
+                              stream=None) -> None:
+    """trtv_verify_dense with the library's static device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check("trtv_verify_dense_noalloc", load().trtv_verify_dense_noalloc(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens), _ptr(out),
+        out_dtype, _stream(stream)))
 
 
 def trtv_msa_proxy_score(geom: Geom, q, kv_pool, page_table, kv_lens, scores, stream=None) -> None:

@@ -17,6 +17,11 @@
 // Per-device error word (TRTV_DEVERR_* bits), set by the kernels.
 __device__ int g_trtv_device_error;
 
+// Scratch of trtv_verify_dense_noalloc (split-KV partials, their log-sum-exp
+// and the split counters), resident on every device that loads the library.
+constexpr size_t kNoAllocScratchBytes = size_t{24} << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace trtv {
 namespace {
 
@@ -27,6 +32,7 @@ constexpr size_t kAlignSlack = 1024;
 std::mutex g_mu;
 int g_sm_count[kMaxDevices];
 int* g_err_ptr[kMaxDevices];
+uint8_t* g_noalloc_ptr[kMaxDevices];
 std::set<std::pair<const void*, int>> g_smem_set;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -58,6 +64,21 @@ int* err_word() {
     g_err_ptr[d] = static_cast<int*>(p);
   }
   return g_err_ptr[d];
+}
+
+// Device address of g_noalloc_scratch on the current device.  The host-side
+// name of the array is only a stand-in: the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+uint8_t* noalloc_scratch() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[d] = static_cast<uint8_t*>(p);
+  }
+  return g_noalloc_ptr[d];
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -450,6 +471,26 @@ trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* 
                               int32_t out_dtype, void* workspace, size_t ws_bytes, void* stream) {
   return attn_common(geom, q, kv_pool, page_table, kv_lens, nullptr, 0, out, out_dtype, workspace,
                      ws_bytes, stream);
+}
+
+trtv_status trtv_verify_dense_noalloc(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                      const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                      int32_t out_dtype, void* stream) {
+  Plan pl;
+  trtv_status s = make_plan(geom, 0, &pl);
+  if (s != TRTV_OK) return s;
+  if (q == nullptr || kv_pool == nullptr || page_table == nullptr || kv_lens == nullptr ||
+      out == nullptr || (out_dtype != TRTV_BF16 && out_dtype != TRTV_F32))
+    return TRTV_ERR_INVALID_ARG;
+  if (pl.ws_total > kNoAllocScratchBytes) return TRTV_ERR_WORKSPACE;  // geometry too large
+  uint8_t* ws = noalloc_scratch();
+  if (ws == nullptr) return TRTV_ERR_CUDA;
+  // the split counters must start at zero; the rest is written before it is read
+  if (cudaMemsetAsync(ws + pl.ws_counters, 0, static_cast<size_t>(pl.num_ctas) * sizeof(int),
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TRTV_ERR_CUDA;
+  return attn_common(geom, q, kv_pool, page_table, kv_lens, nullptr, 0, out, out_dtype, ws,
+                     kNoAllocScratchBytes, stream);
 }
 
 trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const void* kv_pool,
