@@ -141,6 +141,13 @@ __device__ __forceinline__ void cursor_next(SeqCursor& cur, const int32_t* scan,
 // o_i / sum_i 2^(lse_i - M) -- writes the rows and resets the counter to zero,
 // leaving the workspace ready for the next call.  Executed by the NTHR
 // threads with threadIdx.x < NTHR, which synchronise on named barrier 1.
+//
+// The partials sit in L2, so the merge is bound by load latency: every
+// thread keeps kMergeChunk contributors x kMergeElems elements of loads in
+// flight before it uses any of them.
+constexpr int kMergeChunk = 8;
+constexpr int kMergeElems = 2;
+
 template <int D, int NTHR = kConsumerWarps * 32>
 __device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t W, float* mlf,
                               int* flag) {
@@ -168,60 +175,107 @@ __device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t
   }
   named_barrier(1, NTHR);
   if (!flag[0]) return;
-  const int c_first = flag[1], c_last = flag[2], first_off = flag[3];
+  const int c_first = flag[1], nc = flag[2] - flag[1] + 1, first_off = flag[3];
   const bool all_ranges = W >= P;
-  auto slot_of = [&](int c, bool& used) -> int64_t {
-    used = all_ranges || cta_unit_begin(c, W, P) < cta_unit_begin(c + 1, W, P);
-    return 2 * static_cast<int64_t>(c) + (c == c_first ? first_off : 0);
+  const int rows = p.rows_pad;
+  // workspace slot of the i-th contributor, -1 when its unit range is empty
+  auto slot_of = [&](int i) -> int64_t {
+    const int c = c_first + i;
+    if (!all_ranges && cta_unit_begin(c, W, P) >= cta_unit_begin(c + 1, W, P)) return -1;
+    return 2 * static_cast<int64_t>(c) + (i == 0 ? first_off : 0);
   };
-  for (int r = tid; r < p.rows_pad; r += NTHR) {
-    float M = -INFINITY;
-    for (int c = c_first; c <= c_last; ++c) {
-      bool used;
-      const int64_t sl = slot_of(c, used);
-      if (used) M = fmaxf(M, __ldcg(p.ws_lse + sl * p.rows_pad + r));
-    }
-    float den = 0.f;
-    if (M != -INFINITY)
-      for (int c = c_first; c <= c_last; ++c) {
-        bool used;
-        const int64_t sl = slot_of(c, used);
-        if (used) den += exp2f(__ldcg(p.ws_lse + sl * p.rows_pad + r) - M);
+  // 1. per row: largest partial log2-sum-exp M and the output scale
+  //    v_scale / sum_i 2^(lse_i - M)
+  for (int r = tid; r < rows; r += NTHR) {
+    float M = -INFINITY, den = 0.f;
+    for (int i0 = 0; i0 < nc; i0 += kMergeChunk) {
+      float x[kMergeChunk];
+#pragma unroll
+      for (int k = 0; k < kMergeChunk; ++k) {
+        const int64_t sl = i0 + k < nc ? slot_of(i0 + k) : -1;
+        x[k] = sl >= 0 ? __ldcg(p.ws_lse + sl * rows + r) : -INFINITY;
       }
+      float m = M;
+#pragma unroll
+      for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, x[k]);
+      if (m != -INFINITY) {
+        den *= exp2f(M - m);
+#pragma unroll
+        for (int k = 0; k < kMergeChunk; ++k) den += exp2f(x[k] - m);
+        M = m;
+      }
+    }
     mlf[2 * r] = M;
     mlf[2 * r + 1] = den > 0.f ? p.v_scale / den : 0.f;
   }
   named_barrier(1, NTHR);
+  // 2. o = scale * sum_i 2^(lse_i - M) o_i, element = (row, 4 head dims)
+  constexpr int F4 = D / 4;
+  const int nel = rows * F4;
   const int64_t obase = static_cast<int64_t>(cur.b) * p.qo_len;
-  for (int e = tid; e < p.rows_pad * (D / 4); e += NTHR) {
-    const int r = e / (D / 4), d = 4 * (e % (D / 4));
-    const int t = r / p.group_pad, gl = r % p.group_pad;
-    if (t >= p.qo_len || gl >= p.group) continue;
-    const float M = mlf[2 * r], inv = mlf[2 * r + 1];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-      for (int c = c_first; c <= c_last; ++c) {
-        bool used;
-        const int64_t sl = slot_of(c, used);
-        if (!used) continue;
-        const float w = exp2f(__ldcg(p.ws_lse + sl * p.rows_pad + r) - M);
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * p.rows_pad + r) * D + d));
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  for (int e0 = 0; e0 < nel; e0 += NTHR * kMergeElems) {
+    int r[kMergeElems], d[kMergeElems];
+    bool ok[kMergeElems];
+    float4 acc[kMergeElems];
+#pragma unroll
+    for (int u = 0; u < kMergeElems; ++u) {
+      const int e = e0 + u * NTHR + tid;
+      r[u] = e / F4;
+      d[u] = 4 * (e % F4);
+      ok[u] = e < nel && r[u] / p.group_pad < p.qo_len && r[u] % p.group_pad < p.group &&
+              mlf[2 * r[u]] != -INFINITY;
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int i0 = 0; i0 < nc; i0 += kMergeChunk) {
+      float x[kMergeElems][kMergeChunk];
+      float4 v[kMergeElems][kMergeChunk];
+#pragma unroll
+      for (int k = 0; k < kMergeChunk; ++k) {
+        const int64_t sl = i0 + k < nc ? slot_of(i0 + k) : -1;
+#pragma unroll
+        for (int u = 0; u < kMergeElems; ++u) {
+          if (sl >= 0 && ok[u]) {
+            x[u][k] = __ldcg(p.ws_lse + sl * rows + r[u]);
+            v[u][k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * rows + r[u]) * D + d[u]));
+          } else {
+            x[u][k] = -INFINITY;
+            v[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeElems; ++u) {
+        const float M = ok[u] ? mlf[2 * r[u]] : 0.f;
+#pragma unroll
+        for (int k = 0; k < kMergeChunk; ++k) {
+          const float w = exp2f(x[u][k] - M);
+          acc[u].x += w * v[u][k].x; acc[u].y += w * v[u][k].y;
+          acc[u].z += w * v[u][k].z; acc[u].w += w * v[u][k].w;
+        }
       }
     }
-    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-    const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(cur.h) * p.group + gl) * D + d;
-    if (p.out_f32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) = acc;
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow) = pk;
+#pragma unroll
+    for (int u = 0; u < kMergeElems; ++u) {
+      const int e = e0 + u * NTHR + tid;
+      if (e >= nel) continue;
+      const int t = r[u] / p.group_pad, gl = r[u] % p.group_pad;
+      if (t >= p.qo_len || gl >= p.group) continue;
+      const float inv = mlf[2 * r[u] + 1];
+      float4 a = acc[u];
+      a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
+      const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(cur.h) * p.group + gl) * D + d[u];
+      if (p.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) = a;
+      } else {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow) = pk;
+      }
     }
   }
-  if (tid == 0) atomicExch(&p.counters[c_last], 0);
+  if (tid == 0) atomicExch(&p.counters[flag[2]], 0);
 }
 
 template <bool FP8, int D, int MT>
