@@ -127,10 +127,9 @@ trtv_status trtv_subpage_view(const trtv_geom* geom, const int32_t* page_table,
  * Workspace bytes that trtv_verify_dense and trtv_msa_sparse_attn need for
  * this geometry (topk = the sparse path's k, 0 for dense only); 0 on invalid
  * geometry.  The workspace is caller-allocated device memory, 256-byte
- * aligned.  Zero-fill it once before its first use (it holds the arrival
- * counters of sequences split across CTAs); every call that completes leaves
- * it zeroed again, so it is reused without further initialisation.  After a
- * call that reported TRTV_DEVERR_TIMEOUT, zero it again.
+ * aligned, with no initial contents required: every call writes each byte it
+ * reads (split-KV partials, split descriptors, the sparse plan) before reading
+ * it.  Calls that may overlap on the GPU must not share a workspace.
  */
 size_t trtv_workspace_bytes(const trtv_geom* geom, int32_t topk);
 
@@ -139,9 +138,9 @@ size_t trtv_workspace_bytes(const trtv_geom* geom, int32_t topk);
  * layers' ladder SDPA mask, identical to decode at qo_len = 1).
  * out[b*T + t][hq][:] = sum_{p <= L_b - T + t} softmax_p(x) v_p, with
  *   x_p = sm_scale * k_scale * (q[b*T + t][hq] . k_p),  v_p scaled by v_scale,
- * k_p / v_p from KV head hq / G of request b.  Split-KV across CTAs with an
- * in-kernel log-sum-exp merge; fp32 accumulation.  out_dtype: TRTV_BF16 or
- * TRTV_F32.
+ * k_p / v_p from KV head hq / G of request b.  Split-KV across CTAs; the
+ * split sequences are merged by log-sum-exp in a second kernel launched on the
+ * same stream; fp32 accumulation.  out_dtype: TRTV_BF16 or TRTV_F32.
  */
 trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* kv_pool,
                               const int32_t* page_table, const int32_t* kv_lens, void* out,
@@ -160,9 +159,8 @@ trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* 
  * 0) exceeds 24 MiB is rejected with TRTV_ERR_WORKSPACE before anything is
  * enqueued.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) -- make that first call before any stream capture.
- * Every call enqueues a cudaMemsetAsync of the split counters and then the
- * attention kernel; it allocates nothing (no cudaMalloc, cudaFree or
- * allocating library routine).  All calls on a device share the one array:
+ * Every call enqueues the same kernels as trtv_verify_dense; it allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).  All calls on a device share the one array:
  * calls that may overlap on the GPU (different streams without ordering)
  * race on it and must not be issued.
  */

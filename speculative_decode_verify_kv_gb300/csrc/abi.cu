@@ -18,7 +18,7 @@
 __device__ int g_trtv_device_error;
 
 // Scratch of trtv_verify_dense_noalloc (split-KV partials, their log-sum-exp
-// and the split counters), resident on every device that loads the library.
+// and the split descriptors), resident on every device that loads the library.
 constexpr size_t kNoAllocScratchBytes = size_t{24} << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -110,7 +110,7 @@ struct Plan {
   int group, group_pad, rows, mt, rows_pad, num_ctas, n_seq;
   int64_t pool_rows;
   // workspace
-  size_t ws_o, ws_lse, ws_counters, ws_blocks, ws_masks, ws_count, ws_total;
+  size_t ws_o, ws_lse, ws_splits, ws_blocks, ws_masks, ws_count, ws_total;
   int plan_cap;
 };
 
@@ -148,8 +148,8 @@ trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
   off = align_up(off + P2 * p.rows_pad * g->head_dim * sizeof(float), 256);
   p.ws_lse = off;
   off = align_up(off + P2 * p.rows_pad * sizeof(float), 256);
-  p.ws_counters = off;
-  off = align_up(off + static_cast<size_t>(ctas) * sizeof(int), 256);
+  p.ws_splits = off;
+  off = align_up(off + static_cast<size_t>(ctas) * sizeof(SplitDesc), 256);
   p.plan_cap = topk > 0 ? std::min(g->qo_len * topk, g->max_pages_per_req) : 0;
   p.ws_blocks = off;
   off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(int32_t), 256);
@@ -363,7 +363,7 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   a.out = out;
   a.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
   a.ws_lse = reinterpret_cast<float*>(wsb + pl.ws_lse);
-  a.counters = reinterpret_cast<int*>(wsb + pl.ws_counters);
+  a.splits = reinterpret_cast<SplitDesc*>(wsb + pl.ws_splits);
   a.plan_blocks = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_blocks) : nullptr;
   a.plan_masks = sparse ? reinterpret_cast<const uint32_t*>(wsb + pl.ws_masks) : nullptr;
   a.plan_count = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_count) : nullptr;
@@ -399,6 +399,8 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
        : g->kv_dtype == TRTV_FP8_E4M3
            ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
            : launch_attn_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  if (e != cudaSuccess) return TRTV_ERR_CUDA;
+  e = launch_combine(g->head_dim, a, st);
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
 }
 
@@ -485,10 +487,6 @@ trtv_status trtv_verify_dense_noalloc(const trtv_geom* geom, const void* q, cons
   if (pl.ws_total > kNoAllocScratchBytes) return TRTV_ERR_WORKSPACE;  // geometry too large
   uint8_t* ws = noalloc_scratch();
   if (ws == nullptr) return TRTV_ERR_CUDA;
-  // the split counters must start at zero; the rest is written before it is read
-  if (cudaMemsetAsync(ws + pl.ws_counters, 0, static_cast<size_t>(pl.num_ctas) * sizeof(int),
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return TRTV_ERR_CUDA;
   return attn_common(geom, q, kv_pool, page_table, kv_lens, nullptr, 0, out, out_dtype, ws,
                      kNoAllocScratchBytes, stream);
 }

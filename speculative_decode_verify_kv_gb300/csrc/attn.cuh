@@ -13,7 +13,8 @@
 // concatenated in sequence order; CTA c takes units [c W / P, (c+1) W / P).
 // A sequence that one CTA covers whole is written as final output; the
 // pieces of a cut sequence are written as (normalised output, log2-sum-exp)
-// partials and merged by the contributor that finishes last (merge_if_last).
+// partials, which the split-combine kernel (combine_kernel) merges right
+// after, on every SM at once.
 //
 // Roles: warp 8 issues TMA tiled loads of each page's K and V sub-pages
 // (128B swizzle) into an NST-stage ring guarded by full/empty mbarriers.
@@ -132,150 +133,33 @@ __device__ __forceinline__ void cursor_next(SeqCursor& cur, const int32_t* scan,
   if ((sparse ? cur.s : cur.b) < n) cursor_fill(cur, scan, Hk, sparse);
 }
 
-// Split-KV merge inside the attention kernel.  A sequence cut between CTAs
-// c_first .. c_last leaves one (normalised output, log2-sum-exp) partial per
-// CTA; each contributor, after writing its partial, counts itself in
-// counters[c_last] (c_last's range starts inside the sequence, so the slot is
-// unique per cut sequence).  The contributor that completes the count merges
-// the partials in CTA order (fixed summation order) -- o = sum_i 2^(lse_i - M)
-// o_i / sum_i 2^(lse_i - M) -- writes the rows and resets the counter to zero,
-// leaving the workspace ready for the next call.  Executed by the NTHR
-// threads with threadIdx.x < NTHR, which synchronise on named barrier 1.
-//
-// The partials sit in L2, so the merge is bound by load latency: every
-// thread keeps kMergeChunk contributors x kMergeElems elements of loads in
-// flight before it uses any of them.
-constexpr int kMergeChunk = 8;
-constexpr int kMergeElems = 2;
-
-template <int D, int NTHR = kConsumerWarps * 32>
-__device__ void merge_if_last(const AttnParams& p, const SeqCursor& cur, int64_t W, float* mlf,
-                              int* flag) {
-  const int tid = threadIdx.x;
-  const int64_t P = p.num_ctas;
-  named_barrier(1, NTHR);  // this CTA's partial rows are written
-  if (tid == 0) {
-    const int64_t c_first = cta_of_unit(cur.start, W, P);
-    const int64_t c_last = cta_of_unit(cur.start + cur.units - 1, W, P);
-    int n = 0;
-    if (W >= P) {
-      n = static_cast<int>(c_last - c_first + 1);  // every CTA range is non-empty
-    } else {
-      for (int64_t c = c_first; c <= c_last; ++c)
-        n += cta_unit_begin(c, W, P) < cta_unit_begin(c + 1, W, P);
-    }
-    __threadfence();
-    const int old = atomicAdd(&p.counters[c_last], 1);
-    const int last = old == n - 1;
-    if (last) __threadfence();
-    flag[0] = last;
-    flag[1] = static_cast<int>(c_first);
-    flag[2] = static_cast<int>(c_last);
-    flag[3] = cta_unit_begin(c_first, W, P) < cur.start ? 1 : 0;  // slot of the first piece
-  }
-  named_barrier(1, NTHR);
-  if (!flag[0]) return;
-  const int c_first = flag[1], nc = flag[2] - flag[1] + 1, first_off = flag[3];
-  const bool all_ranges = W >= P;
-  const int rows = p.rows_pad;
-  // workspace slot of the i-th contributor, -1 when its unit range is empty
-  auto slot_of = [&](int i) -> int64_t {
-    const int c = c_first + i;
-    if (!all_ranges && cta_unit_begin(c, W, P) >= cta_unit_begin(c + 1, W, P)) return -1;
-    return 2 * static_cast<int64_t>(c) + (i == 0 ? first_off : 0);
-  };
-  // 1. per row: largest partial log2-sum-exp M and the output scale
-  //    v_scale / sum_i 2^(lse_i - M)
-  for (int r = tid; r < rows; r += NTHR) {
-    float M = -INFINITY, den = 0.f;
-    for (int i0 = 0; i0 < nc; i0 += kMergeChunk) {
-      float x[kMergeChunk];
-#pragma unroll
-      for (int k = 0; k < kMergeChunk; ++k) {
-        const int64_t sl = i0 + k < nc ? slot_of(i0 + k) : -1;
-        x[k] = sl >= 0 ? __ldcg(p.ws_lse + sl * rows + r) : -INFINITY;
-      }
-      float m = M;
-#pragma unroll
-      for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, x[k]);
-      if (m != -INFINITY) {
-        den *= exp2f(M - m);
-#pragma unroll
-        for (int k = 0; k < kMergeChunk; ++k) den += exp2f(x[k] - m);
-        M = m;
-      }
-    }
-    mlf[2 * r] = M;
-    mlf[2 * r + 1] = den > 0.f ? p.v_scale / den : 0.f;
-  }
-  named_barrier(1, NTHR);
-  // 2. o = scale * sum_i 2^(lse_i - M) o_i, element = (row, 4 head dims)
-  constexpr int F4 = D / 4;
-  const int nel = rows * F4;
-  const int64_t obase = static_cast<int64_t>(cur.b) * p.qo_len;
-  for (int e0 = 0; e0 < nel; e0 += NTHR * kMergeElems) {
-    int r[kMergeElems], d[kMergeElems];
-    bool ok[kMergeElems];
-    float4 acc[kMergeElems];
-#pragma unroll
-    for (int u = 0; u < kMergeElems; ++u) {
-      const int e = e0 + u * NTHR + tid;
-      r[u] = e / F4;
-      d[u] = 4 * (e % F4);
-      ok[u] = e < nel && r[u] / p.group_pad < p.qo_len && r[u] % p.group_pad < p.group &&
-              mlf[2 * r[u]] != -INFINITY;
-      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int i0 = 0; i0 < nc; i0 += kMergeChunk) {
-      float x[kMergeElems][kMergeChunk];
-      float4 v[kMergeElems][kMergeChunk];
-#pragma unroll
-      for (int k = 0; k < kMergeChunk; ++k) {
-        const int64_t sl = i0 + k < nc ? slot_of(i0 + k) : -1;
-#pragma unroll
-        for (int u = 0; u < kMergeElems; ++u) {
-          if (sl >= 0 && ok[u]) {
-            x[u][k] = __ldcg(p.ws_lse + sl * rows + r[u]);
-            v[u][k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * rows + r[u]) * D + d[u]));
-          } else {
-            x[u][k] = -INFINITY;
-            v[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kMergeElems; ++u) {
-        const float M = ok[u] ? mlf[2 * r[u]] : 0.f;
-#pragma unroll
-        for (int k = 0; k < kMergeChunk; ++k) {
-          const float w = exp2f(x[u][k] - M);
-          acc[u].x += w * v[u][k].x; acc[u].y += w * v[u][k].y;
-          acc[u].z += w * v[u][k].z; acc[u].w += w * v[u][k].w;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kMergeElems; ++u) {
-      const int e = e0 + u * NTHR + tid;
-      if (e >= nel) continue;
-      const int t = r[u] / p.group_pad, gl = r[u] % p.group_pad;
-      if (t >= p.qo_len || gl >= p.group) continue;
-      const float inv = mlf[2 * r[u] + 1];
-      float4 a = acc[u];
-      a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
-      const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(cur.h) * p.group + gl) * D + d[u];
-      if (p.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) = a;
-      } else {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow) = pk;
-      }
+// Stream-K bookkeeping for the split-combine kernel.  CTA k (k >= 1) starts at
+// unit B_k = begin(k).  If B_k falls strictly inside a sequence that began in
+// CTA k - 1's range (B_{k-1} <= start < B_k), boundary k is the first one that
+// cuts it: CTA k records the sequence and its contributors c_first = k - 1 ..
+// cta_of_unit(start + units - 1).  Every boundary is recorded (b = -1 when it
+// starts no cut), so each cut sequence is described exactly once per call.
+// Called by one thread of every CTA, before any early exit.
+__device__ __forceinline__ void write_split_desc(const AttnParams& p, const int32_t* scan, int n, int Hk,
+                                                 bool sparse, int64_t W) {
+  const int64_t k = blockIdx.x, P = p.num_ctas;
+  if (k == 0 || k >= P) return;
+  SplitDesc d;
+  d.b = -1; d.h = 0; d.c_first = 0; d.nc = 0; d.first_off = 0; d.pad = 0;
+  d.W = W;
+  const int64_t B = cta_unit_begin(k, W, P);
+  if (B < W) {
+    const SeqCursor cur = cursor_first(scan, n, Hk, sparse, B);
+    const int64_t Bp = cta_unit_begin(k - 1, W, P);
+    if (cur.start < B && cur.start >= Bp) {
+      d.b = cur.b;
+      d.h = cur.h;
+      d.c_first = static_cast<int>(k - 1);
+      d.nc = static_cast<int>(cta_of_unit(cur.start + cur.units - 1, W, P) - (k - 1) + 1);
+      d.first_off = Bp < cur.start ? 1 : 0;
     }
   }
-  if (tid == 0) atomicExch(&p.counters[flag[2]], 0);
+  p.splits[k] = d;
 }
 
 template <bool FP8, int D, int MT>
@@ -323,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return 0;
   });
   const int64_t W = item_start(scan, nitems, Hk, sparse);
+  if (threadIdx.x == 0) write_split_desc(p, scan, nitems, Hk, sparse, W);
+  pdl_trigger();  // the split-combine kernel may be scheduled now
   // rows of sequences with no units (invalid request, or no selected block)
   // are zero: CTA c clears items c, c + P, ...
   for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
@@ -721,7 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_barrier(1, kConsumerWarps * 32);
       }
     }
-    if (!whole) merge_if_last<D>(p, cur, W, mlf, reinterpret_cast<int*>(ml));
   }
 }
 

@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     return 0;
   });
   const int64_t W = item_start(scan, nitems, Hk, sparse);
+  if (threadIdx.x == 0) write_split_desc(p, scan, nitems, Hk, sparse, W);
+  pdl_trigger();  // the split-combine kernel may be scheduled now
   for (int i = blockIdx.x; i < nitems; i += gridDim.x) {  // zero rows of empty sequences
     if (scan[i + 1] != scan[i]) continue;
     const int b = sparse ? i / Hk : i;
@@ -428,7 +430,6 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         }
       }
       tc_fence_before();
-      if (!whole) merge_if_last<D, 256>(p, cur, W, ml + 256, reinterpret_cast<int*>(ml));
     }
   }
 

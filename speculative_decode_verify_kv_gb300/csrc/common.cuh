@@ -31,6 +31,16 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
 
 // ---- parameter blocks ----------------------------------------------------
 
+// One CTA boundary of the stream-K split: the sequence (request b, KV head h)
+// whose units it cuts first, its contributing CTAs c_first .. c_first + nc - 1
+// and the workspace slot offset of the first piece; b = -1 when the boundary
+// starts no cut.  Written by the attention CTA that starts at the boundary,
+// read by the split-combine kernel.
+struct SplitDesc {
+  int b, h, c_first, nc, first_off, pad;
+  long long W;  // total units of the call
+};
+
 struct AttnParams {
   const __nv_bfloat16* q;
   const int32_t* page_table;
@@ -38,7 +48,7 @@ struct AttnParams {
   void* out;
   float* ws_o;          // [2 * num_ctas, rows_pad, D] partial outputs
   float* ws_lse;        // [2 * num_ctas, rows_pad] partial log2-sum-exp
-  int* counters;        // [num_ctas] arrivals per cut sequence, zero between calls
+  SplitDesc* splits;    // [num_ctas] boundary k's cut sequence (entry 0 unused)
   const int32_t* plan_blocks;   // sparse: [n_seq, plan_cap] selected blocks
   const uint32_t* plan_masks;   // sparse: [n_seq, plan_cap] token bitmasks
   const int32_t* plan_count;    // sparse: [n_seq]
@@ -67,6 +77,15 @@ struct ProxyParams {
 };
 
 // ---- small helpers -------------------------------------------------------
+
+// Programmatic dependent launch: let the next kernel of the stream start
+// (trigger), and wait until the previous one has finished and its writes are
+// visible (wait; a no-op when the kernel was launched without the attribute).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -39,6 +39,10 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
                         int num_kv_heads, int max_pages, int topk, int32_t* out, int* err,
                         cudaStream_t st);
 
+// Split-KV combine of the cut sequences, launched right after an attention
+// kernel with programmatic dependent launch (no-op for a single CTA).
+cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st);
+
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_attr(const void* func, size_t bytes);
 

@@ -4,6 +4,9 @@
 //                         the bitmask of verify tokens that selected each
 //   topk_kernel           warp-level per-token top-k (radix select), ties to
 //                         the lower block index, ascending output
+//   combine_kernel        split-KV combine: merges the (normalised output,
+//                         log2-sum-exp) partials of every sequence that the
+//                         attention kernel's stream-K split cut
 #include "common.cuh"
 #include "launch.h"
 
@@ -218,6 +221,121 @@ __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __r
 // ---------------------------------------------------------------------------
 // host launchers
 
+
+// ---------------------------------------------------------------------------
+// Split-KV combine.  The attention over a sequence cut into pieces i with
+// partial outputs o_i (each normalised by its own softmax sum) and log2-sum-exp
+// lse_i equals softmax over the union: o = sum_i 2^(lse_i - M) o_i /
+// sum_i 2^(lse_i - M), M = max_i lse_i (the ladder and sparse passes of
+// "... verify" attend each row's visible positions exactly once, whichever
+// piece holds them).  One CTA per (CTA boundary k, chunk of 8 rows for
+// head_dim 128, 16 for 64; one float4 per thread): boundary k's
+// descriptor names the cut sequence it starts (or none); contributors are
+// summed in CTA order, so the result does not depend on timing.  Launched with
+// programmatic dependent launch right after the attention kernel: the CTAs
+// wait (pdl_wait) until that kernel has finished and its partials are visible.
+constexpr int kCombineThreads = 256;
+// rows per CTA: one float4 of one row per thread
+__host__ __device__ constexpr int combine_rows(int D) { return kCombineThreads * 4 / D; }
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int F4 = D / 4;         // float4 per row
+  constexpr int R = combine_rows(D);  // rows of this CTA's chunk
+  constexpr int EL = R * F4 / kCombineThreads;  // elements per thread (1)
+  constexpr int CU = 4;             // contributors per batch of loads
+  __shared__ int4 desc[2];
+  __shared__ int slots[kMaxCombineParts];
+  pdl_wait();
+  const int nch = p.rows_pad / R;
+  const int k = 1 + blockIdx.x / nch, chunk = blockIdx.x % nch;
+  const int tid = threadIdx.x;
+  if (tid < 2) desc[tid] = __ldcg(reinterpret_cast<const int4*>(p.splits + k) + tid);
+  __syncthreads();
+  // SplitDesc as two int4: {b, h, c_first, nc}, {first_off, pad, W low, W high}
+  const int b = desc[0].x, h = desc[0].y, c_first = desc[0].z, nc = desc[0].w;
+  if (b < 0) return;
+  const int64_t W = static_cast<int64_t>(static_cast<uint32_t>(desc[1].z)) |
+                    (static_cast<int64_t>(desc[1].w) << 32);
+  const int64_t P = p.num_ctas;
+  for (int i = tid; i < nc; i += kCombineThreads) {
+    const int64_t c = c_first + i;
+    const bool used = W >= P || cta_unit_begin(c, W, P) < cta_unit_begin(c + 1, W, P);
+    slots[i] = used ? static_cast<int>(2 * c + (i == 0 ? desc[1].x : 0)) : -1;
+  }
+  __syncthreads();
+  const int rows = p.rows_pad, r0 = chunk * R, s0 = slots[0];  // the first piece always exists
+  // one pass per element (row, 4 head dims), online over the contributors:
+  // m = running max lse_i, l = sum 2^(lse_i - m), acc = sum 2^(lse_i - m) o_i
+  int r[EL], d[EL];
+  float m[EL], l[EL];
+  float4 acc[EL];
+#pragma unroll
+  for (int u = 0; u < EL; ++u) {
+    const int e = u * kCombineThreads + tid;
+    r[u] = r0 + e / F4;
+    d[u] = 4 * (e % F4);
+    m[u] = -INFINITY;
+    l[u] = 0.f;
+    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i0 = 0; i0 < nc; i0 += CU) {
+    float x[EL][CU];
+    float4 v[EL][CU];
+#pragma unroll
+    for (int j = 0; j < CU; ++j) {
+      const int sl = i0 + j < nc ? slots[i0 + j] : -1;
+      const int64_t sa = sl >= 0 ? sl : s0;
+#pragma unroll
+      for (int u = 0; u < EL; ++u) {
+        x[u][j] = __ldcg(p.ws_lse + sa * rows + r[u]);
+        v[u][j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sa * rows + r[u]) * D + d[u]));
+        if (sl < 0) x[u][j] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < EL; ++u) {
+      float mn = m[u];
+#pragma unroll
+      for (int j = 0; j < CU; ++j) mn = fmaxf(mn, x[u][j]);
+      if (mn == -INFINITY) continue;
+      const float sc = exp2f(m[u] - mn);
+      l[u] *= sc;
+      acc[u].x *= sc; acc[u].y *= sc; acc[u].z *= sc; acc[u].w *= sc;
+#pragma unroll
+      for (int j = 0; j < CU; ++j) {
+        if (x[u][j] == -INFINITY) continue;
+        const float w = exp2f(x[u][j] - mn);
+        l[u] += w;
+        acc[u].x += w * v[u][j].x; acc[u].y += w * v[u][j].y;
+        acc[u].z += w * v[u][j].z; acc[u].w += w * v[u][j].w;
+      }
+      m[u] = mn;
+    }
+  }
+  const int64_t obase = static_cast<int64_t>(b) * p.qo_len;
+#pragma unroll
+  for (int u = 0; u < EL; ++u) {
+    const int t = r[u] / p.group_pad, gl = r[u] % p.group_pad;
+    if (t >= p.qo_len || gl >= p.group) continue;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);  // no visible position in any piece
+    if (l[u] > 0.f) {
+      const float inv = p.v_scale / l[u];
+      a = make_float4(acc[u].x * inv, acc[u].y * inv, acc[u].z * inv, acc[u].w * inv);
+    }
+    const int64_t orow = ((obase + t) * p.num_q_heads + static_cast<int64_t>(h) * p.group + gl) * D + d[u];
+    if (p.out_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) = a;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow) = pk;
+    }
+  }
+}
+
 cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t* k_sub,
                                 int32_t* v_sub, int batch, int qo_len, int max_pages,
                                 int num_slots, int stride, int* err, cudaStream_t st) {
@@ -255,6 +373,22 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
   topk_kernel<<<blocks, 256, 0, st>>>(scores, lens, batch, qo_len, num_kv_heads, max_pages, topk,
                                       out, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st) {
+  if (p.num_ctas < 2) return cudaSuccess;  // no CTA boundary, nothing is cut
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((p.num_ctas - 1) * (p.rows_pad / combine_rows(head_dim))));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_kernel<64>, p)
+                        : cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
 }
 
 }  // namespace trtv

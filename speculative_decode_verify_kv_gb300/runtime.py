@@ -44,8 +44,8 @@ class DeviceVerify:
         self.ws_bytes = trtv_workspace_bytes(self.geom, max(self.topk, 0))
         if self.ws_bytes == 0:
             raise RuntimeError("geometry rejected by trtv_workspace_bytes")
-        # zeroed once: it holds the split-sequence arrival counters
-        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+        # no initial contents needed: each call writes what it reads
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.scores = torch.empty(B, T, Hk, NP, dtype=torch.float32, device=dev)
         k = max(self.topk, 1)
         self.block_idx = torch.empty(B, T, Hk, k, dtype=torch.int32, device=dev)

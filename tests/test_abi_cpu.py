@@ -67,8 +67,8 @@ def test_geometry_validation(lib, over, status):
 def test_workspace_size_and_checks(lib):
     g = geom()
     need = lib.trtv_workspace_bytes(ctypes.byref(g), 0)
-    # 2 partial slots per CTA x 16 padded rows x (64 outputs + 1 lse) floats + one counter
-    # per CTA, each region 256-byte aligned
+    # 2 partial slots per CTA x 16 padded rows x (64 outputs + 1 lse) floats + one 32-byte
+    # split descriptor per CTA, each region 256-byte aligned
     assert need == 2 * 4 * 16 * 64 * 4 + 512 + 256
     need_sparse = lib.trtv_workspace_bytes(ctypes.byref(g), 2)
     assert need_sparse > need

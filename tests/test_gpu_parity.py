@@ -100,6 +100,37 @@ def test_dense_split_invariance(num_ctas):
     assert (dv1.out - o2).abs().max().item() < 5e-3
 
 
+@pytest.mark.parametrize("num_ctas", [40, 100, 1024])
+def test_dense_one_sequence_over_many_ctas(num_ctas):
+    """One (request, KV head) sequence of 63 pages cut among up to 40 CTAs (more
+    contributors than a warp has lanes), or among 100 / 1024 CTAs of which
+    most get no page (empty ranges leave no partial)."""
+    p = W.make_problem(kv_lens=[8000], qo_len=4, num_q_heads=8, num_kv_heads=1, head_dim=128,
+                       seed=13, slack_slots=2)
+    check_dense(p, num_ctas=num_ctas, out_dtype="f32")
+
+
+def test_workspace_needs_no_initial_contents():
+    """A workspace full of 0xFF bytes (NaN partials, -1 descriptors) gives the
+    same results: every call writes what it reads."""
+    p = W.make_problem(kv_lens=[1000, 37, 513, 4, 2000], qo_len=4, num_q_heads=64, num_kv_heads=4,
+                       head_dim=128, seed=17, slack_slots=5, topk=4, max_pages_per_req=16)
+    dv = DeviceVerify(p, num_ctas=9, out_dtype="f32")
+    dv.workspace.fill_(255)
+    out = dv.dense().cpu().numpy()
+    ref, _ = oracle.verify_dense(oracle.Inputs(p))
+    assert np.abs(out - ref).max() <= TOL_BF16
+    dv.workspace.fill_(255)
+    dv.proxy()
+    idx = dv.select()
+    dv.workspace.fill_(255)
+    sp = dv.sparse().cpu().numpy()
+    ref, bad = oracle.sparse_attn(oracle.Inputs(p), idx.cpu().numpy())
+    assert bad == 0
+    assert np.abs(sp - ref).max() <= TOL_BF16
+    assert T.trtv_get_device_error() == 0
+
+
 @pytest.mark.parametrize("Hq,Hk,Tq,D", [
     (8, 8, 4, 128),    # G = 1
     (16, 1, 4, 128),   # G = 16, 64 rows
