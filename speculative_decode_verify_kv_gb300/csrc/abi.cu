@@ -244,34 +244,41 @@ bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
 }
 
 bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
-  const size_t qbuf = 128 * 128 * 2;
+  // Q tile: rows x 128 head dims of bf16 in two 64-column halves; at most 64
+  // rows take 16 KB (the M = 128 UMMA then reads rows 64..127 from whatever
+  // follows the tile -- the K ring -- into accumulator rows nobody reads)
+  const size_t qbuf = pl.group * g->qo_len <= 64 ? 64 * 128 * 2 : 128 * 128 * 2;
   const size_t kv = static_cast<size_t>(kGroups) * 2 * kBox;
   const int nitems = sparse ? pl.n_seq : g->batch;
   const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
   const size_t ml = 1280 * sizeof(float);
-  // one Q tile, two K stages, three V stages: V stages are held longest (until
-  // PV retires), so they get the depth
-  const int nq = kUmmaAttnQTiles, nk = kUmmaAttnKStages, nv = kUmmaAttnVStages;
-  size_t off = 0;
-  a->off_q = 0;
-  off += nq * qbuf;
-  a->off_stage = static_cast<int>(off);
-  a->stage_bytes = static_cast<int>(kv);
-  off += nk * kv;
-  a->off_vring = static_cast<int>(off);
-  off += nv * kv;
-  a->off_scan = static_cast<int>(off);
-  off += scan;
-  a->off_ml = static_cast<int>(off);
-  off += ml;
-  a->off_bar = static_cast<int>(align_up(off, 8));
-  off = a->off_bar + (2 * nk + 2 * nv + 16) * sizeof(uint64_t) + 16;
-  a->nstages = nk;
-  a->nv = nv;
-  a->nq = nq;
-  a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
-  *bytes = off + kAlignSlack;
-  return *bytes <= kSmemOptin;
+  const int nq = kUmmaAttnQTiles, nv = kUmmaAttnVStages;
+  // K stages are freed by QK, V stages only by PV, so V gets its depth first;
+  // a third K stage when it fits
+  for (int nk = kUmmaAttnKStagesMax; nk >= 2; --nk) {
+    size_t off = 0;
+    a->off_q = 0;
+    off += nq * qbuf;
+    a->off_stage = static_cast<int>(off);
+    a->stage_bytes = static_cast<int>(kv);
+    off += nk * kv;
+    a->off_vring = static_cast<int>(off);
+    off += nv * kv;
+    a->off_scan = static_cast<int>(off);
+    off += scan;
+    a->off_ml = static_cast<int>(off);
+    off += ml;
+    a->off_bar = static_cast<int>(align_up(off, 8));
+    off = a->off_bar + (2 * nk + 2 * nv + 16) * sizeof(uint64_t) + 16;
+    a->nstages = nk;
+    a->nv = nv;
+    a->nq = nq;
+    a->qbuf = static_cast<int>(qbuf);
+    a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
+    *bytes = off + kAlignSlack;
+    if (*bytes <= kSmemOptin) return true;
+  }
+  return false;
 }
 
 // The tcgen05 proxy covers bf16, head_dim 128, a power-of-two group <= 16 with

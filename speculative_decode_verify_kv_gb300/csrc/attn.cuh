@@ -314,13 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t j = j0; j < j1; ++j, ++it) {
       const int st = it % NST;
       const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
-      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, p.err));
+      // plan entry loaded before the wait: its latency overlaps the TMA
       int blk = static_cast<int>(j);
       uint32_t tokmask = 0xffffffffu;
       if (sparse) {
         blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
         tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
       }
+      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, p.err));
       const int pos0 = blk * kPage;
       int bnd[2];
 #pragma unroll

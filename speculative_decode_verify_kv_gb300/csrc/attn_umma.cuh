@@ -21,11 +21,13 @@
 //                   row's maximum rises by more than 8; the stale maximum is
 //                   exact since the final division uses the same one),
 //                   P = 2^(x - m) as bf16 pairs stored back over S[buf]
-//   O += P V        16 UMMA 128x64x16 with A = P in TMEM and B = the V page
-//                   (token rows, MN-major) -> TMEM O (fp32, 128 columns)
+//   O += P V        8 UMMA 128x128x16 with A = P in TMEM and B = the V page
+//                   (token rows, MN-major, both 64-column halves in one
+//                   instruction) -> TMEM O (fp32, 128 columns)
 // Warp 8 streams Q (3-D box per sequence) and the K pages, warp 10 the V pages
 // (two rings of 32 KB stages in the UMMA's 128B-swizzled layout, each stream
-// as far ahead as its own ring allows); warp 9 lane 0 issues the
+// as far ahead as its own ring allows: three V stages, and three K stages when
+// the Q tile has at most 64 rows and takes 16 KB); warp 9 lane 0 issues the
 // UMMAs, QK of page i + 1 ahead of PV of page i so the tensor core overlaps
 // the softmax (the last PV of a sequence is not held back).  TMEM: three S
 // buffers at columns 0, 128, 256 and O at 384.
@@ -47,15 +49,14 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
                      const __grid_constant__ AttnParams p) {
   static_assert(D == 128, "tcgen05 attention handles head_dim 128");
   constexpr int KV = kGroups * 2 * kBox;  // one page of K (or V) for one head: 32 KB
-  constexpr int QBUF = 128 * D * 2;
   constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 128);
-  constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 64) | (1u << 16);  // B (V) MN-major
+  constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
   constexpr uint32_t TM_O = 384;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int NK = p.nstages, NV = p.nv, NQ = p.nq;
+  const int NK = p.nstages, NV = p.nv, NQ = p.nq, QBUF = p.qbuf;
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* kempty = kfull + NK;   // QK finished reading the K stage
   uint64_t* vfull = kempty + NK;
@@ -216,11 +217,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         const uint32_t v0 = smem_u32(vring + vs * KV);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-            umma_bf16_tmem_a(tmem + TM_O + hb * 64, tmem + b * 128 + kk * 8,
-                             umma_desc_sw128_mn(v0 + hb * (KV / 2) + kk * 2048), IDESC_PV,
-                             (!first || kk > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tmem + TM_O, tmem + b * 128 + kk * 8, umma_desc_sw128_mn(v0 + kk * 2048, KV / 2),
+                           IDESC_PV, (!first || kk > 0) ? 1u : 0u);
         umma_commit(&vempty[vs]);
         umma_commit(&pvdone[b]);
       };
@@ -285,15 +283,17 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       float m_use = -INFINITY, l = 0.f;
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int buf = it % kSBufs;
-        if (!dead)
-          dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, p.err));
-        tc_fence_after();
+        // the page's plan entry is loaded before the wait, so its latency
+        // overlaps the QK rather than the softmax
         int blk = static_cast<int>(j);
         uint32_t tokmask = 0xffffffffu;
         if (sparse) {
           blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
           tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
         }
+        if (!dead)
+          dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, p.err));
+        tc_fence_after();
         const int pos0 = blk * kPage;
         if (live) {
           const int bnd = (valid && ((tokmask >> t) & 1u)) ? bound : -1;

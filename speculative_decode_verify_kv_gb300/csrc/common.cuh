@@ -22,11 +22,12 @@ constexpr int kGroups = 4;        // sub-pages per page
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kBox = 4096;        // bytes of one TMA box: 32 rows x 128 B
-constexpr int kMaxCombineParts = 1024;
-// tcgen05 attention pipeline depth (32 KB each: Q tiles, K pages, V pages)
+constexpr int kMaxCombineParts = 1024;  // upper bound on num_ctas
+// tcgen05 attention pipeline depth: one Q tile (16 KB for at most 64 rows,
+// else 32 KB), K and V pages of 32 KB (three K stages when they fit)
 constexpr int kUmmaAttnQTiles = 1;
-constexpr int kUmmaAttnKStages = 2;
-constexpr int kUmmaAttnVStages = 3;  // upper bound on num_ctas
+constexpr int kUmmaAttnKStagesMax = 3;
+constexpr int kUmmaAttnVStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
 
 // ---- parameter blocks ----------------------------------------------------
@@ -61,6 +62,7 @@ struct AttnParams {
   // dynamic shared memory carve-up (byte offsets from the 1024-aligned base)
   int off_stage, stage_bytes, off_k, off_v, off_conv, off_merge, off_ml, off_scan, off_bar;
   int off_q, off_vring, nv, nq;  // tcgen05 kernel: Q tiles (nq), V ring (nv); K ring at off_stage, nstages
+  int qbuf;                      // tcgen05 kernel: bytes of one Q tile (rows x 256)
 };
 
 struct ProxyParams {

@@ -119,12 +119,14 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
 }
 
 // Shared-memory descriptor of an MN-major bf16 operand in the same
-// 128B-swizzled rows (here: V, one row of 64 head dims per token).  Used with
-// N = 64 (one swizzle atom wide), so only the 1024-byte step between 8-row
-// groups along K matters; both offsets carry it.
-__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t saddr) {
+// 128B-swizzled rows (here: V, one row of 64 head dims per token in each of
+// the tile's two 64-column halves).  Along K (tokens) the 8-row groups are
+// 1024 bytes apart (stride byte offset); along N the 64-column swizzle atoms
+// are `atom_stride` bytes apart (leading byte offset), so one N = 128 UMMA
+// covers both halves.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t saddr, uint32_t atom_stride) {
   uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1024 >> 4) << 16;
+  d |= static_cast<uint64_t>(atom_stride >> 4) << 16;
   d |= static_cast<uint64_t>(1024 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
