@@ -393,6 +393,9 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   a.num_ctas = pl.num_ctas;
   a.scale_log2 = g->sm_scale * g->k_scale * 1.4426950408889634f;
   a.v_scale = g->v_scale;
+  // stream-K charge per sequence start, in pages: what a sequence switch costs
+  // each kernel relative to one page of K and V
+  a.setup = umma ? kUmmaSeqSetup : kSeqSetup;
   cudaError_t e;
   if (sparse) {
     e = launch_sparse_plan(block_idx, lens, g->batch, g->qo_len, g->num_kv_heads,

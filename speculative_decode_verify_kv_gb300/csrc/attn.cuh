@@ -133,11 +133,56 @@ __device__ __forceinline__ void cursor_next(SeqCursor& cur, const int32_t* scan,
   if ((sparse ? cur.s : cur.b) < n) cursor_fill(cur, scan, Hk, sparse);
 }
 
+// Stream-K with a setup charge: every non-empty sequence owns `setup` virtual
+// units ahead of its pages (or blocks), standing for the fixed cost of
+// starting it (epilogue of the previous one, Q, pipeline refill), so a CTA
+// that starts more sequences gets fewer pages.  A sequence spans virtual
+// units [start, start + units); its real units begin at rs = start + setup.
+__device__ __forceinline__ bool seq_in_range(const SeqCursor& c, int64_t u1, int setup) {
+  return c.start + setup < u1;
+}
+// real units [j0, j1) of the sequence inside the CTA's range [u0, u1)
+__device__ __forceinline__ int64_t seq_j0(const SeqCursor& c, int64_t u0, int setup) {
+  const int64_t rs = c.start + setup;
+  return (u0 > rs ? u0 : rs) - rs;
+}
+__device__ __forceinline__ int64_t seq_j1(const SeqCursor& c, int64_t u1, int setup) {
+  const int64_t e = c.start + c.units;
+  return (u1 < e ? u1 : e) - (c.start + setup);
+}
+// no other CTA holds a real unit of the sequence
+__device__ __forceinline__ bool seq_whole(const SeqCursor& c, int64_t u0, int64_t u1, int setup) {
+  return u0 <= c.start + setup && c.start + c.units <= u1;
+}
+// workspace slot of a cut piece: 2c for the piece that began before the CTA's
+// range (at most one), 2c + 1 for the one that runs past it (at most one)
+__device__ __forceinline__ int64_t seq_slot(const SeqCursor& c, int64_t u0, int setup) {
+  return 2 * static_cast<int64_t>(blockIdx.x) + (c.start + setup <= u0 ? 0 : 1);
+}
+
+// Virtual units of item i (a request's per-KV-head page count, or a sparse
+// sequence's block count) plus the setup charge; 0 for an empty item.
+__device__ __forceinline__ int32_t seq_units(const AttnParams& p, int i, int T, bool sparse) {
+  int32_t u;
+  if (sparse) {
+    u = p.plan_count[i];
+  } else {
+    const int L = p.kv_lens[i];
+    if (len_valid(L, T, p.max_pages)) {
+      u = (L + kPage - 1) / kPage;
+    } else {
+      if (blockIdx.x == 0) atomicOr(p.err, TRTV_DEVERR_KV_LEN);
+      u = 0;
+    }
+  }
+  return u > 0 ? u + p.setup : 0;
+}
+
 // Stream-K bookkeeping for the split-combine kernel.  CTA k (k >= 1) starts at
-// unit B_k = begin(k).  If B_k falls strictly inside a sequence that began in
-// CTA k - 1's range (B_{k-1} <= start < B_k), boundary k is the first one that
-// cuts it: CTA k records the sequence and its contributors c_first = k - 1 ..
-// cta_of_unit(start + units - 1).  Every boundary is recorded (b = -1 when it
+// unit B_k = begin(k).  If B_k falls strictly inside the real units of a
+// sequence whose real units began in CTA k - 1's range (B_{k-1} <= rs < B_k),
+// boundary k is the first one that cuts it: CTA k records the sequence and its
+// contributors c_first = k - 1 .. cta_of_unit(start + units - 1).  Every boundary is recorded (b = -1 when it
 // starts no cut), so each cut sequence is described exactly once per call.
 // Called by one thread of every CTA, before any early exit.
 __device__ __forceinline__ void write_split_desc(const AttnParams& p, const int32_t* scan, int n, int Hk,
@@ -151,12 +196,13 @@ __device__ __forceinline__ void write_split_desc(const AttnParams& p, const int3
   if (B < W) {
     const SeqCursor cur = cursor_first(scan, n, Hk, sparse, B);
     const int64_t Bp = cta_unit_begin(k - 1, W, P);
-    if (cur.start < B && cur.start >= Bp) {
+    const int64_t rs = cur.start + p.setup;  // first real unit
+    if (rs < B && rs >= Bp) {
       d.b = cur.b;
       d.h = cur.h;
       d.c_first = static_cast<int>(k - 1);
       d.nc = static_cast<int>(cta_of_unit(cur.start + cur.units - 1, W, P) - (k - 1) + 1);
-      d.first_off = Bp < cur.start ? 1 : 0;
+      d.first_off = Bp < rs ? 1 : 0;
     }
   }
   p.splits[k] = d;
@@ -200,11 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   block_exclusive_scan(nitems, scan, warp_tot, [&](int i) -> int32_t {
-    if (sparse) return p.plan_count[i];
-    const int L = p.kv_lens[i];
-    if (len_valid(L, T, p.max_pages)) return (L + kPage - 1) / kPage;
-    if (blockIdx.x == 0) atomicOr(p.err, TRTV_DEVERR_KV_LEN);
-    return 0;
+    return seq_units(p, i, T, sparse);
   });
   const int64_t W = item_start(scan, nitems, Hk, sparse);
   if (threadIdx.x == 0) write_split_desc(p, scan, nitems, Hk, sparse, W);
@@ -239,10 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     bool alive = true;
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-         alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+         alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
          cursor_next(cur, scan, nitems, Hk, sparse)) {
-      const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
-      const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+      const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int st = it % NST;
         const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
@@ -288,11 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it = 0;
 
   for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-       (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+       (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
        cursor_next(cur, scan, nitems, Hk, sparse)) {
     const int b = cur.b, h = cur.h;
-    const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
-    const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+    const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
     const int L = p.kv_lens[b];
 
     uint32_t qa[KS][4];
@@ -500,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 2);
     l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 1);
     l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 2);
-    const bool whole = u0 <= cur.start && cur.start + cur.units <= u1;
-    const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (cur.start <= u0 ? 0 : 1);
+    const bool whole = seq_whole(cur, u0, u1, p.setup);
+    const int64_t slot = seq_slot(cur, u0, p.setup);
     const int64_t obase = static_cast<int64_t>(b) * T;
 
     if constexpr (NSL == 1) {

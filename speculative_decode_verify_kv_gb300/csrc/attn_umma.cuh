@@ -94,11 +94,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     fence_mbar_init();
   }
   block_exclusive_scan(nitems, scan, warp_tot, [&](int i) -> int32_t {
-    if (sparse) return p.plan_count[i];
-    const int L = p.kv_lens[i];
-    if (len_valid(L, T, p.max_pages)) return (L + kPage - 1) / kPage;
-    if (blockIdx.x == 0) atomicOr(p.err, TRTV_DEVERR_KV_LEN);
-    return 0;
+    return seq_units(p, i, T, sparse);
   });
   const int64_t W = item_start(scan, nitems, Hk, sparse);
   if (threadIdx.x == 0) write_split_desc(p, scan, nitems, Hk, sparse, W);
@@ -151,7 +147,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       int it = 0, sq = 0;
       bool alive = true;
       for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-           alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+           alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
         if (!is_v) {
           const int qb = sq % NQ;
@@ -168,8 +164,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
                 "r"(smem_u32(&qfull[qb]))
                 : "memory");
         }
-        const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
-        const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+        const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
         for (int64_t j = j0; j < j1; ++j, ++it) {
           const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
                                  : static_cast<int>(j);
@@ -225,13 +220,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       int it = 0, sq = 0, pend = -1;
       bool pend_first = false;
       for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-           alive && (sparse ? cur.s : cur.b) < nitems && cur.start < u1;
+           alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
         const int qb = sq % NQ;
         if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err)) { alive = false; break; }
         const uint32_t a0 = smem_u32(qbase + qb * QBUF);
-        const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
-        const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+        const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
         for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
           const int ks = it % NK, buf = it % kSBufs;
           if (!mbar_wait(&kfull[ks], static_cast<uint32_t>(it / NK) & 1u, p.err) ||
@@ -275,11 +269,10 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     bool dead = false;
     int it = 0;
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-         (sparse ? cur.s : cur.b) < nitems && cur.start < u1; cursor_next(cur, scan, nitems, Hk, sparse)) {
+         (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup); cursor_next(cur, scan, nitems, Hk, sparse)) {
       const int L = p.kv_lens[cur.b];
       const int bound = valid ? L - T + t : -1;
-      const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
-      const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
+      const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
       float m_use = -INFINITY, l = 0.f;
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int buf = it % kSBufs;
@@ -378,8 +371,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       if (!dead)
         dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last % kSBufs], static_cast<uint32_t>(last / kSBufs) & 1u, p.err));
       tc_fence_after();
-      const bool whole = u0 <= cur.start && cur.start + cur.units <= u1;
-      const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (cur.start <= u0 ? 0 : 1);
+      const bool whole = seq_whole(cur, u0, u1, p.setup);
+      const int64_t slot = seq_slot(cur, u0, p.setup);
       if (live) {
         xl[hf * 128 + r] = l;
         named_barrier(2 + q, 64);

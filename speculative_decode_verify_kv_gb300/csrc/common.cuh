@@ -29,6 +29,9 @@ constexpr int kUmmaAttnQTiles = 1;
 constexpr int kUmmaAttnKStagesMax = 3;
 constexpr int kUmmaAttnVStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
+// stream-K setup charge per sequence, in units (pages or blocks)
+constexpr int kSeqSetup = 2;       // mma.sync attention
+constexpr int kUmmaSeqSetup = 1;   // tcgen05 attention
 
 // ---- parameter blocks ----------------------------------------------------
 
@@ -63,6 +66,7 @@ struct AttnParams {
   int off_stage, stage_bytes, off_k, off_v, off_conv, off_merge, off_ml, off_scan, off_bar;
   int off_q, off_vring, nv, nq;  // tcgen05 kernel: Q tiles (nq), V ring (nv); K ring at off_stage, nstages
   int qbuf;                      // tcgen05 kernel: bytes of one Q tile (rows x 256)
+  int setup;                     // virtual units charged per sequence start (stream-K weight)
 };
 
 struct ProxyParams {
