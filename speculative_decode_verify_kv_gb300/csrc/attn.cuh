@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  pdl_wait();  // inputs may come from the previous kernel of the stream
   block_exclusive_scan(nitems, scan, warp_tot, [&](int i) -> int32_t {
     return seq_units(p, i, T, sparse);
   });

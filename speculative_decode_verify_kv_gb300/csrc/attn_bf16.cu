@@ -11,8 +11,7 @@ static cudaError_t go_attn(const CUtensorMap& map, const AttnParams& p, int grid
   const void* fn = reinterpret_cast<const void*>(&attn_kernel<false, D, MT>);
   cudaError_t e = ensure_smem_attr(fn, smem);
   if (e != cudaSuccess) return e;
-  attn_kernel<false, D, MT><<<grid, kThreads, smem, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel<false, D, MT>, dim3(grid), dim3(kThreads), smem, st, map, p);
 }
 
 cudaError_t launch_attn_bf16(int head_dim, int mt, const CUtensorMap& map, const AttnParams& p, int grid,
@@ -40,8 +39,7 @@ cudaError_t launch_attn_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map
   const void* fn = reinterpret_cast<const void*>(&attn_umma_kernel<128>);
   cudaError_t e = ensure_smem_attr(fn, smem);
   if (e != cudaSuccess) return e;
-  attn_umma_kernel<128><<<grid, kUmmaAttnThreads, smem, st>>>(kv_map, q_map, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_umma_kernel<128>, dim3(grid), dim3(kUmmaAttnThreads), smem, st, kv_map, q_map, p);
 }
 
 }  // namespace trtv

@@ -10,8 +10,7 @@ static cudaError_t go_attn(const CUtensorMap& map, const AttnParams& p, int grid
   const void* fn = reinterpret_cast<const void*>(&attn_kernel<true, D, MT>);
   cudaError_t e = ensure_smem_attr(fn, smem);
   if (e != cudaSuccess) return e;
-  attn_kernel<true, D, MT><<<grid, kThreads, smem, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel<true, D, MT>, dim3(grid), dim3(kThreads), smem, st, map, p);
 }
 
 cudaError_t launch_attn_fp8(int head_dim, int mt, const CUtensorMap& map, const AttnParams& p, int grid,

@@ -43,6 +43,26 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
 // kernel with programmatic dependent launch (no-op for a single CTA).
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st);
 
+// Launch with programmatic dependent launch: the kernel may be scheduled while
+// the previous kernel of the stream is still running (once that one has
+// triggered), and every kernel of the library calls pdl_wait() before it reads
+// or writes global memory that the previous kernel may touch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_attr(const void* func, size_t bytes);
 

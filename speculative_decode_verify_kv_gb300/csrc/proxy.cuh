@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Hk = p.num_kv_heads, T = p.qo_len, NST = p.nstages, NP = p.max_pages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  pdl_wait();  // inputs may come from the previous kernel of the stream
   // -inf for every score no page pass writes: pages past the request's last
   // page (all pages of an invalid request).
   {
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return 0;
   });
   const int64_t W = static_cast<int64_t>(scan[p.batch]) * Hk;
+  pdl_trigger();
   if (W == 0) return;
   const int64_t u0 = cta_unit_begin(blockIdx.x, W, p.num_ctas);
   const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);

@@ -11,8 +11,7 @@ static cudaError_t go_proxy(const CUtensorMap& map, const ProxyParams& p, int gr
   const void* fn = reinterpret_cast<const void*>(&proxy_kernel<false, D, MT>);
   cudaError_t e = ensure_smem_attr(fn, smem);
   if (e != cudaSuccess) return e;
-  proxy_kernel<false, D, MT><<<grid, kThreads, smem, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(proxy_kernel<false, D, MT>, dim3(grid), dim3(kThreads), smem, st, map, p);
 }
 
 cudaError_t launch_proxy_bf16(int head_dim, int mt, const CUtensorMap& map, const ProxyParams& p, int grid,
@@ -40,8 +39,7 @@ cudaError_t launch_proxy_umma(const CUtensorMap& kv_map, const CUtensorMap& q_ma
   const void* fn = reinterpret_cast<const void*>(&proxy_umma_kernel<128>);
   cudaError_t e = ensure_smem_attr(fn, smem);
   if (e != cudaSuccess) return e;
-  proxy_umma_kernel<128><<<grid, kUmmaProxyThreads, smem, st>>>(kv_map, q_map, p);
-  return cudaGetLastError();
+  return launch_pdl(proxy_umma_kernel<128>, dim3(grid), dim3(kUmmaProxyThreads), smem, st, kv_map, q_map, p);
 }
 
 }  // namespace trtv

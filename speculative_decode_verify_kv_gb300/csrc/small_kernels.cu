@@ -22,6 +22,8 @@ __global__ void subpage_view_kernel(const int32_t* __restrict__ pt, const int32_
                                     int32_t* __restrict__ k_sub, int32_t* __restrict__ v_sub,
                                     int batch, int qo_len, int max_pages, int num_slots, int stride,
                                     int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int nsub = kGroups * max_pages;
   const int64_t total = static_cast<int64_t>(batch) * nsub;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
@@ -56,6 +58,8 @@ __global__ void sparse_plan_kernel(const int32_t* __restrict__ idx, const int32_
   extern __shared__ uint32_t mask[];  // [max_pages]
   __shared__ uint32_t bad_tokens;
   __shared__ int32_t warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x, b = s / num_kv_heads, h = s % num_kv_heads;
   const int T = qo_len, L = lens[b];
   if (!len_valid(L, T, max_pages)) {
@@ -136,6 +140,8 @@ __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __r
                             int batch, int qo_len, int num_kv_heads, int max_pages, int topk,
                             int32_t* __restrict__ out, int* err) {
   __shared__ uint32_t hist_all[8][256];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   const int64_t nrows = static_cast<int64_t>(batch) * qo_len * num_kv_heads;
@@ -247,6 +253,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   __shared__ int4 desc[2];
   __shared__ int slots[kMaxCombineParts];
   pdl_wait();
+  pdl_trigger();
   const int nch = p.rows_pad / R;
   const int k = 1 + blockIdx.x / nch, chunk = blockIdx.x % nch;
   const int tid = threadIdx.x;
@@ -343,9 +350,8 @@ cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t*
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 4096 ? (want > 0 ? want : 1) : 4096);
-  subpage_view_kernel<<<blocks, threads, 0, st>>>(pt, lens, k_sub, v_sub, batch, qo_len, max_pages,
-                                                  num_slots, stride, err);
-  return cudaGetLastError();
+  return launch_pdl(subpage_view_kernel, dim3(blocks), dim3(threads), 0, st, pt, lens, k_sub, v_sub, batch,
+                    qo_len, max_pages, num_slots, stride, err);
 }
 
 cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
@@ -359,10 +365,9 @@ cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batc
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  sparse_plan_kernel<<<batch * num_kv_heads, 256, smem, st>>>(
-      idx, lens, batch, qo_len, num_kv_heads, max_pages, topk, plan_cap, plan_blocks, plan_masks,
-      plan_count, err);
-  return cudaGetLastError();
+  return launch_pdl(sparse_plan_kernel, dim3(batch * num_kv_heads), dim3(256), smem, st, idx, lens, batch,
+                    qo_len, num_kv_heads, max_pages, topk, plan_cap, plan_blocks, plan_masks, plan_count,
+                    err);
 }
 
 cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int qo_len,
@@ -370,25 +375,15 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
                         cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(batch) * qo_len * num_kv_heads;
   const int blocks = static_cast<int>((rows + 7) / 8);
-  topk_kernel<<<blocks, 256, 0, st>>>(scores, lens, batch, qo_len, num_kv_heads, max_pages, topk,
-                                      out, err);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(blocks), dim3(256), 0, st, scores, lens, batch, qo_len, num_kv_heads,
+                    max_pages, topk, out, err);
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st) {
   if (p.num_ctas < 2) return cudaSuccess;  // no CTA boundary, nothing is cut
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((p.num_ctas - 1) * (p.rows_pad / combine_rows(head_dim))));
-  cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_kernel<64>, p)
-                        : cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
+  const dim3 grid(static_cast<unsigned>((p.num_ctas - 1) * (p.rows_pad / combine_rows(head_dim))));
+  return head_dim == 64 ? launch_pdl(combine_kernel<64>, grid, dim3(kCombineThreads), 0, st, p)
+                        : launch_pdl(combine_kernel<128>, grid, dim3(kCombineThreads), 0, st, p);
 }
 
 }  // namespace trtv
