@@ -30,7 +30,7 @@ constexpr int kUmmaAttnKStagesMax = 3;
 constexpr int kUmmaAttnVStages = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
 // stream-K setup charge per sequence, in units (pages or blocks)
-constexpr int kSeqSetup = 2;       // mma.sync attention
+constexpr int kSeqSetup = 3;       // mma.sync attention
 constexpr int kUmmaSeqSetup = 1;   // tcgen05 attention
 
 // ---- parameter blocks ----------------------------------------------------
