@@ -73,6 +73,9 @@ def _bind(h: ctypes.CDLL) -> ctypes.CDLL:
     h.trtvo_proxy_score.argtypes = [P, vp, vp, vp, vp, vp]
     h.trtvo_topk.argtypes = [P, vp, vp, ctypes.c_int, vp]
     h.trtvo_sparse_attn.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_int, vp]
+    h.trtvo_e4m3_from_float.restype = ctypes.c_uint8
+    h.trtvo_e4m3_from_float.argtypes = [ctypes.c_float]
+    h.trtvo_stage_kv.argtypes = [P, vp, vp, vp, vp, vp]
     h.trtvo_num_threads.restype = ctypes.c_int
     return h
 
@@ -207,6 +210,20 @@ class Oracle:
         bad = self.h.trtvo_sparse_attn(ctypes.byref(P), _ptr(x.q), _ptr(x.pool), _ptr(x.pt),
                                       _ptr(x.lens), _ptr(idx), k, _ptr(out))
         return out, bad
+
+    def e4m3_from_float(self, x: float) -> int:
+        return int(self.h.trtvo_e4m3_from_float(x))
+
+    def stage_kv(self, x: Inputs, k_new, v_new):
+        """Stage the qo_len new tokens' K and V ([B*T, Hk, D] bf16) into a copy
+        of the pool; returns (new pool, requests not staged)."""
+        P = x.P
+        kn = _np(k_new, np.uint16)
+        vn = _np(v_new, np.uint16)
+        pool = x.pool.copy()
+        bad = self.h.trtvo_stage_kv(ctypes.byref(P), _ptr(kn), _ptr(vn), _ptr(x.pt), _ptr(x.lens),
+                                    _ptr(pool))
+        return pool, bad
 
     def num_threads(self) -> int:
         return self.h.trtvo_num_threads()

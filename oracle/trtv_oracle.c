@@ -407,6 +407,85 @@ int trtvo_sparse_attn(const trtvo_problem* P, const uint16_t* q, const void* poo
     return bad;
 }
 
+/* ---- KV slot staging along the ladder ----------------------------------- */
+
+/* Encoding of a binary32 value as OCP E4M3 with round-to-nearest-even and
+ * saturation to the largest finite magnitude (448): the finite code of the
+ * same sign whose value is nearest to x; on a tie, the code with the even
+ * (zero) last mantissa bit.  NaN maps to the NaN code S.1111.111; +-inf and
+ * every |x| above 448 map to +-448.  Written as a search over the 127 finite
+ * codes of each sign, each decoded by the definition above. */
+uint8_t trtvo_e4m3_from_float(float x) {
+    if (isnan(x)) return 0x7F;
+    int neg = signbit(x) ? 1 : 0;
+    double ax = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c < 0x7F; ++c) {          /* 0x00 .. 0x7E: +0 .. +448 */
+        double v = trtvo_e4m3_to_double((uint8_t)c);
+        double err = fabs(v - ax);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(best | (neg << 7));
+}
+
+/* KV slot staging ("... verify" commit of fork PR #3: KV slot staging
+ * generalizes to the causal ladder).  Token t of request b is verify token t,
+ * whose K and V go to position p = kv_len - qo_len + t of the request: slot
+ * s = page_table[b][p / 128], element offset by the layout rule above, for
+ * every KV head h and head dim d:
+ *   K[p][h][d] <- k_new[b * qo_len + t][h][d],  V likewise from v_new.
+ * bf16 caches store the bf16 bits unchanged.  FP8 caches store
+ * E4M3(x / scale) with x the bf16 value, the quotient taken in binary32
+ * (scale = k_scale for K, v_scale for V) and encoded as above.
+ * A request is staged only when qo_len <= kv_len <= 128 * max_pages and the
+ * page(s) holding positions kv_len - qo_len .. kv_len - 1 name slots of the
+ * pool; otherwise nothing of it is written.  Returns the number of requests
+ * not staged. */
+int trtvo_stage_kv(const trtvo_problem* P, const uint16_t* k_new, const uint16_t* v_new,
+                   const int32_t* pt, const int32_t* lens, void* pool) {
+    const int T = P->qo_len, Hk = P->num_kv_heads, D = P->head_dim;
+    int bad = 0;
+    for (int b = 0; b < P->batch; ++b) {
+        const int32_t L = lens[b];
+        int ok = L >= T && (int64_t)L <= (int64_t)TRTVO_PAGE * P->max_pages_per_req;
+        if (ok) {
+            for (int t = 0; t < T; ++t) {
+                int32_t s = pt[(int64_t)b * P->max_pages_per_req + (L - T + t) / TRTVO_PAGE];
+                if (s < 0 || s >= P->num_slots) ok = 0;
+            }
+        }
+        if (!ok) {
+            ++bad;
+            continue;
+        }
+        for (int t = 0; t < T; ++t) {
+            const int64_t p = (int64_t)L - T + t;
+            const int64_t slot = pt[(int64_t)b * P->max_pages_per_req + p / TRTVO_PAGE];
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint16_t* src = kv == 0 ? k_new : v_new;
+                const float scale = (float)(kv == 0 ? P->k_scale : P->v_scale);
+                for (int h = 0; h < Hk; ++h)
+                    for (int d = 0; d < D; ++d) {
+                        const uint16_t bits = src[(((int64_t)b * T + t) * Hk + h) * D + d];
+                        const int64_t off = trtvo_element_offset(slot, P->slot_stride, Hk, D, p, h, kv, d);
+                        if (P->kv_dtype == TRTVO_FP8_E4M3) {
+                            const float x = (float)trtvo_bf16_to_double(bits);
+                            const float q = x / scale;
+                            ((uint8_t*)pool)[off] = trtvo_e4m3_from_float(q);
+                        } else {
+                            ((uint16_t*)pool)[off] = bits;
+                        }
+                    }
+            }
+        }
+    }
+    return bad;
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int trtvo_num_threads(void) {
 #ifdef _OPENMP

@@ -455,4 +455,134 @@ def check_sparse_single_block_vs_sdpa(orc):
                 assert np.allclose(o, ref, rtol=0, atol=1e-12), (blk, t, hq)
 
 
+# ---------------------------------------------------------------------------
+# KV slot staging along the ladder
+
+def _e4m3_values():
+    """Value of every finite E4M3 code via torch's float8 conversion."""
+    v = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return {c: v[c] for c in range(256) if not math.isnan(v[c])}
+
+
+def check_e4m3_encode_roundtrip_ties_saturation(orc):
+    vals = _e4m3_values()
+    for c, v in vals.items():                       # every finite code (both zeros) round-trips
+        assert orc.e4m3_from_float(v) == c, (hex(c), v)
+    pos = sorted((v, c) for c, v in vals.items() if c < 0x80)
+    for (v0, c0), (v1, c1) in zip(pos, pos[1:]):
+        mid = (v0 + v1) / 2                         # exact in binary32
+        even = c0 if (c0 & 1) == 0 else c1          # ties go to the even mantissa
+        assert orc.e4m3_from_float(mid) == even, (v0, v1)
+        assert orc.e4m3_from_float(-mid) == even | 0x80, (v0, v1)
+        below = float(np.nextafter(np.float32(mid), np.float32(-1)))
+        above = float(np.nextafter(np.float32(mid), np.float32(1e9)))
+        assert orc.e4m3_from_float(below) == c0 and orc.e4m3_from_float(above) == c1, (v0, v1)
+    for x in (449.0, 464.0, 480.0, 1e6, float("inf")):   # saturation to +-448
+        assert orc.e4m3_from_float(x) == 0x7E and orc.e4m3_from_float(-x) == 0xFE, x
+    assert orc.e4m3_from_float(float("nan")) == 0x7F
+    rng = np.random.default_rng(9)                  # in-range values vs torch's conversion
+    xs = np.concatenate([rng.standard_normal(2000) * s for s in (1e-3, 0.1, 1.0, 30.0, 140.0)])
+    xs = xs[np.abs(xs) <= 448].astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for x, r in zip(xs, ref):
+        assert orc.e4m3_from_float(float(x)) == r, (x, r)
+
+
+def _staging_problem(seed, dtype, stride, lens, T=4, Hk=2, D=32, scale=None):
+    kw = {}
+    if scale is not None:
+        kw = dict(k_scale=scale, v_scale=2 * scale)
+    p = small(seed=seed, lens=lens, T=T, Hq=2 * Hk, Hk=Hk, D=D, stride=stride, kv_dtype=dtype)
+    if kw:
+        p = p.with_(**kw)
+    g = torch.Generator().manual_seed(seed + 1)
+    k_new = torch.randn(p.batch * T, Hk, D, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(p.batch * T, Hk, D, generator=g).to(torch.bfloat16)
+    return p, k_new, v_new
+
+
+def _expected_staged(p, k_new, v_new):
+    """The pool after staging, written with the independent layout formulation:
+    the request's tokens as contiguous [L, Hk, D] rows, the last qo_len rows
+    replaced (encoded with torch's float8 conversion for FP8 caches), scattered
+    back through numpy reshape / transpose."""
+    pool5 = pool5_of(p).copy()
+    pt = p.page_table.numpy()
+    T = p.qo_len
+    for b in range(p.batch):
+        L = int(p.kv_lens[b])
+        if L < T:
+            continue
+        for kv, new in ((0, k_new), (1, v_new)):
+            rows = gather_contiguous(pool5, pt, p.slot_stride, b, L, kv)
+            x = new[b * T:(b + 1) * T].to(torch.float32)
+            if p.kv_dtype == W.FP8:
+                sc = torch.tensor(p.k_scale if kv == 0 else p.v_scale, dtype=torch.float32)
+                enc = (x / sc).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            else:
+                enc = new[b * T:(b + 1) * T].view(torch.int16).numpy().view(np.uint16)
+            rows[L - T:L] = enc
+            scatter_contiguous(pool5, pt, p.slot_stride, b, rows, kv)
+    return pool5
+
+
+def check_stage_kv_vs_independent_layout(orc):
+    for seed, dtype, stride, scale in ((31, W.BF16, 2, None), (32, W.BF16, 5, None),
+                                       (33, W.FP8, 2, 0.02), (34, W.FP8, 3, 0.3)):
+        p, k_new, v_new = _staging_problem(seed, dtype, stride, (5, 127, 128, 129, 300, 260), scale=scale)
+        pool, bad = orc.stage_kv(O.Inputs(p), k_new, v_new)
+        assert bad == 0
+        want = _expected_staged(p, k_new, v_new)
+        assert np.array_equal(pool.reshape(want.shape), want), (seed, dtype, stride)
+
+
+def check_stage_kv_then_gather_reads_new_rows(orc):
+    p, k_new, v_new = _staging_problem(35, W.BF16, 2, (7, 130))
+    x = O.Inputs(p)
+    pool, _ = orc.stage_kv(x, k_new, v_new)
+    x2 = O.Inputs(p, pool=torch.from_numpy(pool.view(np.int16)).view(torch.bfloat16))
+    T, Hk = p.qo_len, p.num_kv_heads
+    for b in range(p.batch):
+        L = int(p.kv_lens[b])
+        for h in range(Hk):
+            K0, V0 = orc.gather_head(x, b, h)
+            K1, V1 = orc.gather_head(x2, b, h)
+            assert np.array_equal(K1[:L - T], K0[:L - T]) and np.array_equal(V1[:L - T], V0[:L - T])
+            kn = k_new[b * T:(b + 1) * T, h].to(torch.float64).numpy()
+            vn = v_new[b * T:(b + 1) * T, h].to(torch.float64).numpy()
+            assert np.array_equal(K1[L - T:], kn) and np.array_equal(V1[L - T:], vn), (b, h)
+
+
+def check_stage_kv_fp8_saturates(orc):
+    p, k_new, v_new = _staging_problem(36, W.FP8, 2, (9,), scale=0.01)
+    big = torch.full_like(k_new, 100.0)             # 100 / 0.01 = 1e4 > 448
+    pool, bad = orc.stage_kv(O.Inputs(p), big, -big)
+    pool5 = pool.reshape(pool5_of(p).shape)
+    pt = p.page_table.numpy()
+    assert bad == 0
+    assert np.all(gather_contiguous(pool5, pt, 2, 0, 9, 0)[5:] == 0x7E)
+    assert np.all(gather_contiguous(pool5, pt, 2, 0, 9, 1)[5:] == 0xFE)
+
+
+def check_stage_kv_skips_invalid_requests(orc):
+    p, k_new, v_new = _staging_problem(37, W.BF16, 2, (3, 200, 40))   # kv_len 3 < qo_len 4
+    pt = p.page_table.clone()
+    pt[2, 0] = p.num_slots + 5                                          # staged page names no slot
+    x = O.Inputs(p, page_table=pt)
+    pool, bad = orc.stage_kv(x, k_new, v_new)
+    assert bad == 2
+    want = pool5_of(p).copy()
+    exp = _expected_staged(p, k_new, v_new)
+    # only request 1 changed
+    pt_np = p.page_table.numpy()
+    for kv in (0, 1):
+        got_rows = gather_contiguous(pool.reshape(want.shape), pt_np, 2, 1, 200, kv)
+        assert np.array_equal(got_rows, gather_contiguous(exp, pt_np, 2, 1, 200, kv))
+    changed = pool.reshape(want.shape) != want
+    for b in (0, 2):
+        for j in range(1):
+            for kv in (0, 1):
+                assert not changed[pt_np[b, j] * 2 + kv].any(), (b, kv)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

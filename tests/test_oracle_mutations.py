@@ -30,6 +30,13 @@ MUTATIONS = [
                                 "for (int p = 0; p < L; ++p) keep[p] = chosen[p / TRTVO_PAGE];"),
                                ("attend_row(P, qv, Kc, Vc, visible, keep, x,", "attend_row(P, qv, Kc, Vc, L, keep, x,")]),
     ("v_scale_on_k", [("double scale = kv == 0 ? P->k_scale : P->v_scale;", "double scale = kv == 0 ? P->v_scale : P->k_scale;")]),
+    ("stage_position_off_by_one", [("const int64_t p = (int64_t)L - T + t;", "const int64_t p = (int64_t)L - T + t - (t == T - 1 ? 0 : -1) - 1;")]),
+    ("stage_k_from_v", [("const uint16_t* src = kv == 0 ? k_new : v_new;", "const uint16_t* src = kv == 0 ? v_new : k_new;")]),
+    ("stage_scale_multiplies", [("const float q = x / scale;", "const float q = x * scale;")]),
+    ("stage_scales_swapped", [("const float scale = (float)(kv == 0 ? P->k_scale : P->v_scale);",
+                               "const float scale = (float)(kv == 0 ? P->v_scale : P->k_scale);")]),
+    ("e4m3_ties_to_lower", [("if (err < best_err || (err == best_err && (c & 1) == 0)) {", "if (err < best_err) {")]),
+    ("e4m3_no_saturation", [("for (int c = 0; c < 0x7F; ++c) {", "if (ax > 448.0) return 0x7F; for (int c = 0; c < 0x7F; ++c) {")]),
 ]
 
 
