@@ -208,6 +208,28 @@ trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const voi
                                  void* stream);
 
 /*
+ * KV slot staging along the ladder (source: PR #3 "... verify" commit: "KV
+ * slot staging generalizes to the causal ladder").  Writes the K and V rows
+ * of the qo_len verify tokens into their cache slots: token t of request b is
+ * position p = kv_len[b] - qo_len + t, stored in slot page_table[b][p / 128]
+ * at the same place the attention entry points read it (K page buffer at
+ * slot * slot_stride, V at slot * slot_stride + 1, grouped-HND sub-page
+ * (p % 128) / 32, row p % 32 of KV head h).
+ *   k_new, v_new  bf16 [batch * qo_len, num_kv_heads, head_dim], row b*T + t,
+ *                 16-byte aligned, caller-owned device memory (read only)
+ *   kv_pool       the pool the attention entry points read (written)
+ * bf16 caches store the bf16 bits; FP8 caches store E4M3(x / k_scale) for K
+ * and E4M3(x / v_scale) for V, the quotient in binary32, rounded to nearest
+ * even and saturated to +-448 (NaN stays NaN).  Nothing else of the pool is
+ * written.  A request whose kv_len is invalid (< qo_len or > 128 *
+ * max_pages_per_req) or whose staged page names no slot of the pool is not
+ * written at all; the device error word gets TRTV_DEVERR_KV_LEN or
+ * TRTV_DEVERR_PAGE_ID.  Host errors as for trtv_verify_dense.
+ */
+trtv_status trtv_stage_kv(const trtv_geom* geom, const void* k_new, const void* v_new, void* kv_pool,
+                          const int32_t* page_table, const int32_t* kv_lens, void* stream);
+
+/*
  * Read and clear the current device's error word (TRTV_DEVERR_* bits).
  * Synchronises `stream`; not for use while capturing a graph.
  */

@@ -19,7 +19,7 @@ __all__ = [
     "TRTV_OK", "TRTV_BF16", "TRTV_FP8_E4M3", "TRTV_F32", "TrtvError", "Geom", "load",
     "trtv_subpage_view", "trtv_workspace_bytes", "trtv_verify_dense", "trtv_msa_proxy_score",
     "trtv_msa_topk", "trtv_msa_sparse_attn", "trtv_get_device_error", "trtv_version",
-    "trtv_verify_dense_noalloc",
+    "trtv_verify_dense_noalloc", "trtv_stage_kv",
     "trtv_status_string", "geom_of", "EXPORTS",
 ]
 
@@ -30,7 +30,7 @@ DEVERR_KV_LEN, DEVERR_PAGE_ID, DEVERR_BLOCK_IDX, DEVERR_TIMEOUT = 1, 2, 4, 8
 # every function the C header declares
 EXPORTS = ("trtv_status_string", "trtv_version", "trtv_subpage_view", "trtv_workspace_bytes",
            "trtv_verify_dense", "trtv_verify_dense_noalloc", "trtv_msa_proxy_score", "trtv_msa_topk",
-           "trtv_msa_sparse_attn", "trtv_get_device_error")
+           "trtv_msa_sparse_attn", "trtv_stage_kv", "trtv_get_device_error")
 
 
 class TrtvError(RuntimeError):
@@ -89,6 +89,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     h.trtv_msa_topk.argtypes = [G, vp, vp, i32, vp, vp]
     h.trtv_msa_sparse_attn.restype = ctypes.c_int
     h.trtv_msa_sparse_attn.argtypes = [G, vp, vp, vp, vp, vp, i32, vp, i32, vp, sz, vp]
+    h.trtv_stage_kv.restype = ctypes.c_int
+    h.trtv_stage_kv.argtypes = [G, vp, vp, vp, vp, vp, vp]
     h.trtv_get_device_error.restype = ctypes.c_int
     h.trtv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
     _lib = h
@@ -183,6 +185,12 @@ def trtv_msa_sparse_attn(geom: Geom, q, kv_pool, page_table, kv_lens, block_idx,
     _check("trtv_msa_sparse_attn", load().trtv_msa_sparse_attn(
         ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens),
         _ptr(block_idx), topk, _ptr(out), out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_stage_kv(geom: Geom, k_new, v_new, kv_pool, page_table, kv_lens, stream=None) -> None:
+    _check("trtv_stage_kv", load().trtv_stage_kv(
+        ctypes.byref(geom), _ptr(k_new), _ptr(v_new), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens),
+        _stream(stream)))
 
 
 def trtv_get_device_error(stream=None) -> int:

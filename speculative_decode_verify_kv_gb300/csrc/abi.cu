@@ -576,6 +576,24 @@ trtv_status trtv_msa_topk(const trtv_geom* g, const float* scores, const int32_t
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
 }
 
+trtv_status trtv_stage_kv(const trtv_geom* g, const void* k_new, const void* v_new, void* kv_pool,
+                          const int32_t* page_table, const int32_t* kv_lens, void* stream) {
+  Plan pl;
+  trtv_status s = make_plan(g, 0, &pl);
+  if (s != TRTV_OK) return s;
+  if (k_new == nullptr || v_new == nullptr || kv_pool == nullptr || page_table == nullptr ||
+      kv_lens == nullptr)
+    return TRTV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv_pool, 16)) return TRTV_ERR_INVALID_ARG;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  const cudaError_t e = launch_stage_kv(k_new, v_new, kv_pool, page_table, kv_lens, g->batch, g->qo_len,
+                                        g->num_kv_heads, g->head_dim, g->max_pages_per_req, g->num_slots,
+                                        g->slot_stride, g->kv_dtype == TRTV_FP8_E4M3, g->k_scale,
+                                        g->v_scale, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+
 trtv_status trtv_get_device_error(int32_t* host_out, void* stream) {
   if (host_out == nullptr) return TRTV_ERR_INVALID_ARG;
   int* err = err_word();

@@ -39,6 +39,12 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
                         int num_kv_heads, int max_pages, int topk, int32_t* out, int* err,
                         cudaStream_t st);
 
+// KV slot staging of the qo_len verify tokens (k_new / v_new: bf16 [B*T, Hk, D]).
+cudaError_t launch_stage_kv(const void* k_new, const void* v_new, void* pool, const int32_t* pt,
+                            const int32_t* lens, int batch, int qo_len, int Hk, int D, int max_pages,
+                            int num_slots, int stride, bool fp8, float k_scale, float v_scale, int* err,
+                            cudaStream_t st);
+
 // Split-KV combine of the cut sequences, launched right after an attention
 // kernel with programmatic dependent launch (no-op for a single CTA).
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st);

@@ -7,6 +7,8 @@
 //   combine_kernel        split-KV combine: merges the (normalised output,
 //                         log2-sum-exp) partials of every sequence that the
 //                         attention kernel's stream-K split cut
+//   stage_kv_kernel       writes the qo_len verify tokens' K and V into their
+//                         cache slots along the ladder
 #include "common.cuh"
 #include "launch.h"
 
@@ -343,6 +345,83 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// KV slot staging ("Eagle3 for M3 MSA path + CUDA graphs compatibility",
+// commit "... verify": KV slot staging generalizes to the causal ladder).
+// Verify token t of request b is cache position p = kv_len - qo_len + t; its
+// K row for KV head h goes to element ((s stride) 4 + (p % 128) / 32)
+// (Hk 32 D) + (h 32 + p % 32) D of the pool, s = page_table[b][p / 128], and
+// its V row to the buffer after (s stride + 1).  bf16 caches take the bits;
+// FP8 caches take E4M3(x / scale) (binary32 quotient, round to nearest even,
+// saturating).  One thread per 16 output bytes.  A request is written only if
+// its kv_len is valid and every staged page names a slot of the pool.
+template <bool FP8>
+__global__ void stage_kv_kernel(const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+                                void* __restrict__ pool, const int32_t* __restrict__ pt,
+                                const int32_t* __restrict__ lens, int batch, int qo_len, int Hk, int D,
+                                int max_pages, int num_slots, int stride, float k_scale, float v_scale,
+                                int* err) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int EPC = FP8 ? 16 : 8;            // elements per 16-byte output chunk
+  const int cpr = D / EPC;                     // chunks per (token, head) row
+  const int64_t total = static_cast<int64_t>(batch) * qo_len * Hk * 2 * cpr;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(e % cpr);
+    int64_t r = e / cpr;
+    const int kv = static_cast<int>(r % 2);
+    r /= 2;
+    const int h = static_cast<int>(r % Hk);
+    const int64_t bt = r / Hk;                 // row of k_new / v_new: b * qo_len + t
+    const int b = static_cast<int>(bt / qo_len), t = static_cast<int>(bt % qo_len);
+    const int L = lens[b];
+    if (!len_valid(L, qo_len, max_pages)) {
+      if (t == 0 && h == 0 && kv == 0 && c == 0) atomicOr(err, TRTV_DEVERR_KV_LEN);
+      continue;
+    }
+    const int first = (L - qo_len) / kPage, last = (L - 1) / kPage;
+    bool ok = true;
+    for (int j = first; j <= last; ++j) {
+      const int sj = pt[static_cast<int64_t>(b) * max_pages + j];
+      ok = ok && sj >= 0 && sj < num_slots;
+    }
+    if (!ok) {
+      if (t == 0 && h == 0 && kv == 0 && c == 0) atomicOr(err, TRTV_DEVERR_PAGE_ID);
+      continue;
+    }
+    const int p = L - qo_len + t;
+    const int64_t s = pt[static_cast<int64_t>(b) * max_pages + p / kPage];
+    const int64_t buffer = s * stride + kv;
+    const int64_t off = ((buffer * kGroups + (p % kPage) / kSub) * Hk + h) * static_cast<int64_t>(kSub) * D +
+                        static_cast<int64_t>(p % kSub) * D + static_cast<int64_t>(c) * EPC;
+    const __nv_bfloat16* src = (kv ? v_new : k_new) + (bt * Hk + h) * static_cast<int64_t>(D) + c * EPC;
+    if constexpr (FP8) {
+      const float scale = kv ? v_scale : k_scale;
+      const uint4 a = *reinterpret_cast<const uint4*>(src);
+      const uint4 bb = *reinterpret_cast<const uint4*>(src + 8);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, bb.x, bb.y, bb.z, bb.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t bits = (w[(4 * i + k) / 2] >> (16 * ((4 * i + k) & 1))) & 0xFFFFu;
+          const float x = __uint_as_float(bits << 16);
+          const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(x / scale, __NV_SATFINITE, __NV_E4M3);
+          packed |= static_cast<uint32_t>(code) << (8 * k);
+        }
+        o[i] = packed;
+      }
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(pool) + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pool) + off) = *reinterpret_cast<const uint4*>(src);
+    }
+  }
+}
+
 cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t* k_sub,
                                 int32_t* v_sub, int batch, int qo_len, int max_pages,
                                 int num_slots, int stride, int* err, cudaStream_t st) {
@@ -384,6 +463,22 @@ cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>((p.num_ctas - 1) * (p.rows_pad / combine_rows(head_dim))));
   return head_dim == 64 ? launch_pdl(combine_kernel<64>, grid, dim3(kCombineThreads), 0, st, p)
                         : launch_pdl(combine_kernel<128>, grid, dim3(kCombineThreads), 0, st, p);
+}
+
+cudaError_t launch_stage_kv(const void* k_new, const void* v_new, void* pool, const int32_t* pt,
+                            const int32_t* lens, int batch, int qo_len, int Hk, int D, int max_pages,
+                            int num_slots, int stride, bool fp8, float k_scale, float v_scale, int* err,
+                            cudaStream_t st) {
+  const int64_t total = static_cast<int64_t>(batch) * qo_len * Hk * 2 * (D / (fp8 ? 16 : 8));
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 4096 ? (want > 0 ? want : 1) : 4096);
+  const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+  const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+  return fp8 ? launch_pdl(stage_kv_kernel<true>, dim3(blocks), dim3(threads), 0, st, kn, vn, pool, pt, lens,
+                          batch, qo_len, Hk, D, max_pages, num_slots, stride, k_scale, v_scale, err)
+             : launch_pdl(stage_kv_kernel<false>, dim3(blocks), dim3(threads), 0, st, kn, vn, pool, pt, lens,
+                          batch, qo_len, Hk, D, max_pages, num_slots, stride, k_scale, v_scale, err);
 }
 
 }  // namespace trtv

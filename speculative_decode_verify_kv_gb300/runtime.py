@@ -14,7 +14,7 @@ from typing import Optional
 
 import torch
 
-from . import (TRTV_BF16, TRTV_F32, geom_of, trtv_msa_proxy_score, trtv_msa_sparse_attn,
+from . import (TRTV_BF16, TRTV_F32, geom_of, trtv_msa_proxy_score, trtv_msa_sparse_attn, trtv_stage_kv,
                trtv_msa_topk, trtv_subpage_view, trtv_verify_dense, trtv_workspace_bytes)
 from .workloads import VerifyProblem
 
@@ -78,6 +78,12 @@ class DeviceVerify:
         trtv_msa_sparse_attn(self.geom, self.q, self.pool, self.page_table, self.kv_lens, idx, k,
                              self.out, self.out_dtype, self.workspace, self.ws_bytes, stream)
         return self.out
+
+    def stage(self, k_new, v_new, stream=None):
+        """Write the qo_len verify tokens' K and V ([B*T, Hk, D] bf16 CUDA
+        tensors) into their cache slots of this problem's pool."""
+        trtv_stage_kv(self.geom, k_new, v_new, self.pool, self.page_table, self.kv_lens, stream)
+        return self.pool
 
     def msa(self, stream=None):
         """The MSA sparse verify pass: proxy scores -> per-token top-k -> sparse attention."""

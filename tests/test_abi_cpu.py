@@ -87,3 +87,14 @@ def test_workspace_size_and_checks(lib):
     big = geom(num_q_heads=64, num_kv_heads=2)  # group 32 > 16: no proxy
     assert lib.trtv_msa_proxy_score(ctypes.byref(big), 16, 16, 16, 16, 16, None) == 2
     assert lib.trtv_get_device_error(None, None) == 1
+
+
+def test_stage_kv_argument_checks(lib):
+    g = geom()
+    # null or misaligned pointers are rejected on the host, before any launch
+    assert lib.trtv_stage_kv(ctypes.byref(g), 0, 16, 16, 16, 16, None) == 1
+    assert lib.trtv_stage_kv(ctypes.byref(g), 16, 16, 0, 16, 16, None) == 1
+    assert lib.trtv_stage_kv(ctypes.byref(g), 8, 16, 16, 16, 16, None) == 1
+    assert lib.trtv_stage_kv(ctypes.byref(g), 16, 16, 24, 16, 16, None) == 1
+    bad = geom(slot_stride=1)
+    assert lib.trtv_stage_kv(ctypes.byref(bad), 16, 16, 16, 16, 16, None) == 1

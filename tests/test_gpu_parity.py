@@ -390,3 +390,52 @@ def test_msa_pipeline_fp8():
     assert np.abs(out - ref).max() <= TOL_FP8
     ref_idx, _ = oracle.topk(x, dv.scores.cpu().numpy().astype(np.float64), p.topk)
     assert np.array_equal(idx, ref_idx)
+
+
+# ---------------------------------------------------------------------------
+# KV slot staging along the ladder (bit-exact against the oracle)
+
+@pytest.mark.parametrize("dtype,stride,D", [(W.BF16, 2, 128), (W.BF16, 8, 64), (W.FP8, 2, 128), (W.FP8, 5, 128)])
+def test_stage_kv_bit_exact(dtype, stride, D):
+    Tq, Hk = 4, 4
+    p = W.make_problem(kv_lens=[1000, 4, 127, 128, 129, 3, 600], qo_len=Tq, num_q_heads=4 * Hk, num_kv_heads=Hk,
+                       head_dim=D, slot_stride=stride, kv_dtype=dtype, seed=51 + stride, slack_slots=3,
+                       max_pages_per_req=8)
+    if dtype == W.FP8:
+        p = p.with_(k_scale=0.013, v_scale=0.021)
+    pt = p.page_table.clone()
+    pt[6, 4] = p.num_slots + 9            # request 6: its staged page names no slot
+    p = p.with_(page_table=pt)
+    g = torch.Generator().manual_seed(7)
+    k_new = (torch.randn(p.batch * Tq, Hk, D, generator=g) * 3).to(torch.bfloat16)
+    v_new = (torch.randn(p.batch * Tq, Hk, D, generator=g) * 3).to(torch.bfloat16)
+    k_new[0, 0, :4] = torch.tensor([1e4, -1e4, float("nan"), 0.0])   # saturation, NaN, zero
+    want, bad = oracle.stage_kv(oracle.Inputs(p), k_new, v_new)
+    assert bad == 2                       # request 5 (kv_len 3 < qo_len) and request 6
+    dv = DeviceVerify(p)
+    dv.stage(k_new.cuda(), v_new.cuda())
+    torch.cuda.synchronize()
+    got = dv.pool.cpu()
+    got = got.view(torch.uint8) if dtype == W.FP8 else got.view(torch.int16)
+    assert np.array_equal(got.numpy().reshape(-1).view(want.dtype), want.reshape(-1)), "pool differs"
+    err = T.trtv_get_device_error()
+    assert err & T.DEVERR_KV_LEN and err & T.DEVERR_PAGE_ID
+
+
+def test_stage_kv_then_verify_reads_the_new_tokens():
+    """Staging followed by the dense verify equals the oracle's verify over the
+    staged pool (the ladder rows see exactly the new keys and values)."""
+    p = W.make_problem(kv_lens=[700, 129, 4000], qo_len=4, num_q_heads=32, num_kv_heads=4, head_dim=128,
+                       seed=57, slack_slots=2)
+    g = torch.Generator().manual_seed(8)
+    k_new = torch.randn(p.batch * 4, 4, 128, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(p.batch * 4, 4, 128, generator=g).to(torch.bfloat16)
+    pool, bad = oracle.stage_kv(oracle.Inputs(p), k_new, v_new)
+    assert bad == 0
+    dv = DeviceVerify(p, out_dtype="f32")
+    dv.stage(k_new.cuda(), v_new.cuda())
+    out = dv.dense().cpu().numpy()
+    staged = torch.from_numpy(pool.view(np.int16)).view(torch.bfloat16).reshape(p.pool.shape)
+    ref, _ = oracle.verify_dense(oracle.Inputs(p, pool=staged))
+    assert np.abs(out - ref).max() <= TOL_BF16
+    assert T.trtv_get_device_error() == 0
