@@ -16,6 +16,8 @@ roofline   the dominant call (trtv_verify_dense: the attention kernel and its
            split-combine kernel) against the measured HBM copy bandwidth;
            algorithmic bytes = K and V of every visible position + Q + O
 cpu_baseline  the fp64 oracle on a bounded sample of the same workload
+stage_kv   trtv_stage_kv (the verify tokens' K/V written into their slots),
+           timed on its own copy of the pool, outside the step
 
 --impl reference runs the fp64 oracle as the reference arm (there is no
 runnable reference implementation; see the design notes).
@@ -261,6 +263,34 @@ def time_path(name, steps, warmup, sampler=None):
     return res
 
 
+def time_stage(name, steps, warmup):
+    """trtv_stage_kv on workload `name`: the qo_len new tokens' K and V of
+    every request written into their cache slots (device-resident inputs)."""
+    import torch
+    from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
+    p = make(name)
+    dv = DeviceVerify(p)
+    g = torch.Generator().manual_seed(99)
+    shape = (p.batch * p.qo_len, p.num_kv_heads, p.head_dim)
+    k_new = torch.randn(shape, generator=g).to(torch.bfloat16).cuda()
+    v_new = torch.randn(shape, generator=g).to(torch.bfloat16).cuda()
+    for _ in range(warmup):
+        dv.stage(k_new, v_new)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        dv.stage(k_new, v_new)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    n = k_new.numel() * 2
+    nbytes = n * 2 + n * p.kv_elem_bytes() + p.batch * 4 * 3
+    del dv
+    torch.cuda.empty_cache()
+    return {"ms": ms, "bytes": int(nbytes), "gbs": nbytes / (ms / 1e3) / 1e9, "launches_per_call": 1}
+
+
 def time_e2e(name, steps, warmup):
     """Same step through the C ABI with host buffers: per step, H2D of q,
     page table and kv_lens from pinned memory, the kernels, D2H of the output."""
@@ -461,10 +491,14 @@ def main():
               "gpu_launches_per_step": r["launches_per_step"]}
         if "unique_blocks_mean" in r:
             pv["unique_blocks_mean"] = r["unique_blocks_mean"]
+        if not pe.topk:
+            pv["stage_kv"] = time_stage(extra, max(10, args.steps // 8), args.warmup)
         paths[extra] = pv
         del r
         _CACHE.pop(extra, None)
         torch.cuda.empty_cache()
+
+    stage = time_stage(args.workload, max(10, args.steps // 8), args.warmup)
 
     e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)
     if dist and e2e:
@@ -486,7 +520,7 @@ def main():
             "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
                     if e2e else None),
             "gpu_launches": head["launches_per_step"] * args.steps, "clocks": clocks,
-            "device_error": head["device_error"], "paths": paths}
+            "device_error": head["device_error"], "paths": paths, "stage_kv": stage}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:
