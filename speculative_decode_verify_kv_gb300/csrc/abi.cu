@@ -235,30 +235,41 @@ bool encode_q_map(const trtv_geom* g, const Plan& pl, const void* q, CUtensorMap
   return r == CUDA_SUCCESS;
 }
 
-// The tcgen05 attention kernel covers bf16, head_dim 128 and a power-of-two
-// group with 32 < group * qo_len <= 128 rows (one UMMA M = 128 tile).
-// Below 33 rows the mma.sync kernel keeps pace with the HBM stream and is used.
+// The tcgen05 attention kernel covers head_dim 128 and a power-of-two group:
+// bf16 caches with 32 < group * qo_len <= 128 rows (one UMMA M = 128 tile;
+// below 33 rows the mma.sync kernel keeps pace with the HBM stream), FP8
+// caches with group * qo_len <= 64 (E4M3 UMMAs read the pages as they are;
+// the lane quadrants without rows host the warps that quantise Q).
 bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
-  return g->kv_dtype == TRTV_BF16 && g->head_dim == 128 && pl.group == pl.group_pad &&
-         pl.group * g->qo_len > 32 && pl.group * g->qo_len <= 128 && aligned(q, 16);
+  if (g->head_dim != 128 || pl.group != pl.group_pad || !aligned(q, 16)) return false;
+  const int rows = pl.group * g->qo_len;
+  if (g->kv_dtype == TRTV_FP8_E4M3) return rows <= 64;
+  return rows > 32 && rows <= 128;
 }
 
 bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
-  // Q tile: rows x 128 head dims of bf16 in two 64-column halves; at most 64
-  // rows take 16 KB (the M = 128 UMMA then reads rows 64..127 from whatever
-  // follows the tile -- the K ring -- into accumulator rows nobody reads)
+  const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
+  // Q tile (as TMA writes it): rows x 128 head dims of bf16 in two 64-column
+  // halves; at most 64 rows take 16 KB (the M = 128 UMMA then reads rows
+  // 64..127 from whatever follows the tile into accumulator rows nobody reads)
   const size_t qbuf = pl.group * g->qo_len <= 64 ? 64 * 128 * 2 : 128 * 128 * 2;
-  const size_t kv = static_cast<size_t>(kGroups) * 2 * kBox;
+  // FP8: the two E4M3 terms of Q (64 rows x 128 B each), right before the K ring
+  const size_t qf8 = fp8 ? 2 * 64 * 128 : 0;
+  const size_t kv = fp8 ? static_cast<size_t>(kGroups) * kBox : static_cast<size_t>(kGroups) * 2 * kBox;
   const int nitems = sparse ? pl.n_seq : g->batch;
   const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
   const size_t ml = 1280 * sizeof(float);
-  const int nq = kUmmaAttnQTiles, nv = kUmmaAttnVStages;
-  // K stages are freed by QK, V stages only by PV, so V gets its depth first;
-  // a third K stage when it fits
-  for (int nk = kUmmaAttnKStagesMax; nk >= 2; --nk) {
+  const int nq = kUmmaAttnQTiles;
+  // bf16: K stages are freed by QK, V stages only by PV, so V gets its depth
+  // first and a third K stage comes when it fits.  FP8: equal rings of 16 KB
+  // stages, as deep as fit.
+  for (int depth = fp8 ? kUmmaAttnFp8Stages : kUmmaAttnKStagesMax; depth >= 2; --depth) {
+    const int nk = depth, nv = fp8 ? depth : kUmmaAttnVStages;
     size_t off = 0;
     a->off_q = 0;
     off += nq * qbuf;
+    a->off_qf8 = static_cast<int>(off);
+    off += qf8;
     a->off_stage = static_cast<int>(off);
     a->stage_bytes = static_cast<int>(kv);
     off += nk * kv;
@@ -269,7 +280,7 @@ bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnPa
     a->off_ml = static_cast<int>(off);
     off += ml;
     a->off_bar = static_cast<int>(align_up(off, 8));
-    off = a->off_bar + (2 * nk + 2 * nv + 16) * sizeof(uint64_t) + 16;
+    off = a->off_bar + (2 * nk + 2 * nv + 24) * sizeof(uint64_t) + 16;
     a->nstages = nk;
     a->nv = nv;
     a->nq = nq;
@@ -405,7 +416,8 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
                            reinterpret_cast<int32_t*>(wsb + pl.ws_count), err, st);
     if (e != cudaSuccess) return TRTV_ERR_CUDA;
   }
-  e = umma ? launch_attn_umma(map, qmap, a, pl.num_ctas, smem, st)
+  e = umma ? (g->kv_dtype == TRTV_FP8_E4M3 ? launch_attn_umma_fp8(map, qmap, a, pl.num_ctas, smem, st)
+                                           : launch_attn_umma(map, qmap, a, pl.num_ctas, smem, st))
        : g->kv_dtype == TRTV_FP8_E4M3
            ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
            : launch_attn_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);

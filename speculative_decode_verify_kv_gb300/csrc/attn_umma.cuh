@@ -42,15 +42,80 @@ constexpr int kUmmaAttnThreads = 352;  // softmax warps 0-7, K/Q TMA 8, UMMA 9, 
 constexpr int kSBufs = 3;
 constexpr uint32_t kAttnTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kQf8Tile = 64 * 128;  // FP8 caches: one E4M3 Q term, 64 rows x 128 B
 
-template <int D>
+// FP8 caches, E4M3 operands with two terms: x ~ hi + lo, hi = E4M3(x),
+// lo = E4M3(x - hi) -- about 8 significant bits, as bf16 (one E4M3 term, 4
+// bits, misses the 5e-2 output tolerance on rows that attend few positions).
+// Two 16-bit values -> the hi and lo E4M3 pairs (low byte = first value).
+__device__ __forceinline__ void split_e4m3x2(__half2 h, uint32_t& hi, uint32_t& lo) {
+  __half2_raw hr = *reinterpret_cast<__half2_raw*>(&h);
+  const __nv_fp8x2_storage_t h8 = __nv_cvt_halfraw2_to_fp8x2(hr, __NV_SATFINITE, __NV_E4M3);
+  __half2_raw back = __nv_cvt_fp8x2_to_halfraw2(h8, __NV_E4M3);
+  const __half2 rest = __hsub2(h, *reinterpret_cast<__half2*>(&back));
+  __half2_raw rr = *reinterpret_cast<const __half2_raw*>(&rest);
+  hi = h8;
+  lo = __nv_cvt_halfraw2_to_fp8x2(rr, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Row r of the bf16 Q tile (two 64-column halves, 128-byte swizzled) -> rows
+// r of the hi and lo E4M3 Q tiles (one 128-byte row each, swizzled) for
+// q / 2^e, 2^e the smallest power of two that brings max |q| of the row to at
+// most 448 (dividing by it is exact).  Returns 2^e, the factor the row's
+// logits are multiplied by.
+__device__ __forceinline__ float quantize_q_row(const uint8_t* qb16, int half_bytes, uint8_t* qhi, uint8_t* qlo,
+                                                int r) {
+  const int sw = r & 7;
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 bf16: half c / 8, chunk c % 8
+    const uint4 v = *reinterpret_cast<const uint4*>(qb16 + (c >> 3) * half_bytes + r * 128 + (((c & 7) ^ sw) << 4));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xFFFF0000u)));
+    }
+  }
+  int e = 0;
+  while (amax > 448.f * exp2f(static_cast<float>(e))) ++e;
+  const float inv = exp2f(static_cast<float>(-e));
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {  // E4M3 chunk c8 = head dims 16 c8 .. + 15 = bf16 chunks 2 c8, 2 c8 + 1
+    uint32_t oh[4], ol[4];
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const int c = 2 * c8 + part;
+      const uint4 v = *reinterpret_cast<const uint4*>(qb16 + (c >> 3) * half_bytes + r * 128 + (((c & 7) ^ sw) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t h0, l0, h1, l1;
+        split_e4m3x2(__floats2half2_rn(__uint_as_float(w[2 * k] << 16) * inv,
+                                       __uint_as_float(w[2 * k] & 0xFFFF0000u) * inv), h0, l0);
+        split_e4m3x2(__floats2half2_rn(__uint_as_float(w[2 * k + 1] << 16) * inv,
+                                       __uint_as_float(w[2 * k + 1] & 0xFFFF0000u) * inv), h1, l1);
+        oh[2 * part + k] = (h0 & 0xFFFFu) | (h1 << 16);
+        ol[2 * part + k] = (l0 & 0xFFFFu) | (l1 << 16);
+      }
+    }
+    *reinterpret_cast<uint4*>(qhi + r * 128 + ((c8 ^ sw) << 4)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+    *reinterpret_cast<uint4*>(qlo + r * 128 + ((c8 ^ sw) << 4)) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+  }
+  return exp2f(static_cast<float>(e));
+}
+
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     attn_umma_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ AttnParams p) {
   static_assert(D == 128, "tcgen05 attention handles head_dim 128");
-  constexpr int KV = kGroups * 2 * kBox;  // one page of K (or V) for one head: 32 KB
-  constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 128);
-  constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
+  // one page of K (or V) for one head: 32 KB of bf16, or 16 KB of E4M3 used as
+  // it is by kind::f8f6f4 UMMAs (Q and P then also E4M3)
+  constexpr int KV = FP8 ? kGroups * kBox : kGroups * 2 * kBox;
+  constexpr uint32_t IDESC_QK = FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(128, 128);
+  constexpr uint32_t IDESC_PV = (FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(128, 128)) |
+                                (1u << 16);  // B (V) MN-major
   constexpr uint32_t TM_O = 384;
 
   extern __shared__ uint8_t smem_raw[];
@@ -67,7 +132,11 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint64_t* qfull = pvdone + kSBufs;    // [2]
   uint64_t* qempty = qfull + 2;    // [2] last QK of the sequence retired
   uint64_t* mdone = qempty + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mdone + 1);
+  // FP8: Q quantised to E4M3 (tile and per-row scales written), and the
+  // softmax warps have read the row scales
+  uint64_t* qcv = mdone + 1;       // [2]
+  uint64_t* qsfree = qcv + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(qsfree + 1);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
   // [0,256) merge flags, [256,512) merge row stats, [512,1024) row maxima of
   // the two column halves (double-buffered by page), [1024,1280) row sums
@@ -77,20 +146,27 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   const int nitems = sparse ? p.batch * Hk : p.batch;
   int32_t* warp_tot = scan + nitems + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // softmax warps of lane quadrants that hold rows; with FP8 the others convert
+  const int live_quads = (G * T + 31) / 32;
+  const int nsoft = FP8 ? 2 * live_quads : 8;        // arrivals on pfull
+  const int nconv = 8 - 2 * live_quads;              // FP8: warps quantising Q
 
   if (threadIdx.x == 0) {
+    const int ncv = nconv > 0 ? nconv : 1;
     for (int i = 0; i < NK; ++i) { mbar_init(&kfull[i], 1); mbar_init(&kempty[i], 1); }
     for (int i = 0; i < NV; ++i) { mbar_init(&vfull[i], 1); mbar_init(&vempty[i], 1); }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&pfull[i], 8);
+      mbar_init(&pfull[i], nsoft);
       mbar_init(&pvdone[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
+      mbar_init(&qcv[i], ncv);
     }
     mbar_init(mdone, 1);
+    mbar_init(qsfree, nsoft);
     fence_mbar_init();
   }
   pdl_wait();  // inputs may come from the previous kernel of the stream
@@ -129,6 +205,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint8_t* qbase = smem + p.off_q;
   uint8_t* kring = smem + p.off_stage;
   uint8_t* vring = smem + p.off_vring;
+  uint8_t* qf8 = smem + p.off_qf8;   // FP8: E4M3 Q tile, [rows][128 B], 128-byte swizzled
+  float* qscale = reinterpret_cast<float*>(smem + p.off_ml);  // FP8: [128] per-row Q scales
 
   if (warp == 8 || warp == 10) {
     // ------------------------------------------- TMA producers: K (+Q) and V
@@ -182,8 +260,10 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           }
           uint8_t* dst = ring + st * KV;
           mbar_arrive_expect_tx(&fullb[st], KV);
+          // bf16: two 128-byte column halves per sub-page; FP8: one box holds
+          // all 128 head dims of a token row
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
+          for (int hb = 0; hb < (FP8 ? 1 : 2); ++hb)
 #pragma unroll
             for (int g = 0; g < kGroups; ++g) {
               const int y = static_cast<int>((buf * kGroups + g) * sub_rows + cur.h * kSub);
@@ -211,10 +291,23 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         }
         tc_fence_after();
         const uint32_t v0 = smem_u32(vring + vs * KV);
+        if constexpr (FP8) {
+          // E4M3: 32 tokens (8 P columns, 32 V rows of 128 B = 4 KB) per UMMA;
+          // all 128 head dims are one 128-byte swizzle atom
+          // O += P_hi V + P_lo V (P_hi in columns 0..31, P_lo in 32..63)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tmem + TM_O, tmem + b * 128 + kk * 8, umma_desc_sw128_mn(v0 + kk * 2048, KV / 2),
-                           IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+          for (int term = 0; term < 2; ++term)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_e4m3_tmem_a(tmem + TM_O, tmem + b * 128 + term * 32 + kk * 8,
+                               umma_desc_sw128_lbo_sbo(v0 + kk * 4096, 1024, 1024), IDESC_PV,
+                               (!first || (term | kk) > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_tmem_a(tmem + TM_O, tmem + b * 128 + kk * 8, umma_desc_sw128_mn(v0 + kk * 2048, KV / 2),
+                             IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&vempty[vs]);
         umma_commit(&pvdone[b]);
       };
@@ -224,7 +317,10 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
            alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
         const int qb = sq % NQ;
-        if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err)) { alive = false; break; }
+        if (!mbar_wait(FP8 ? &qcv[qb] : &qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err)) {
+          alive = false;
+          break;
+        }
         const uint32_t a0 = smem_u32(qbase + qb * QBUF);
         const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
         for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
@@ -236,10 +332,23 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           }
           tc_fence_after();
           const uint32_t k0 = smem_u32(kring + ks * KV);
+          if constexpr (FP8) {
+            // E4M3: a 128-byte row holds all 128 head dims; K = 32 per UMMA;
+            // S = Q_hi K^T + Q_lo K^T
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            umma_bf16(tmem + buf * 128, umma_desc_sw128(a0 + (k >> 2) * (QBUF / 2) + (k & 3) * 32),
-                      umma_desc_sw128(k0 + (k >> 2) * (KV / 2) + (k & 3) * 32), IDESC_QK, k > 0);
+            for (int term = 0; term < 2; ++term) {
+              const uint32_t q0 = smem_u32(qf8 + term * kQf8Tile);
+#pragma unroll
+              for (int k = 0; k < D / 32; ++k)
+                umma_e4m3(tmem + buf * 128, umma_desc_sw128(q0 + k * 32), umma_desc_sw128(k0 + k * 32), IDESC_QK,
+                          (term | k) > 0);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              umma_bf16(tmem + buf * 128, umma_desc_sw128(a0 + (k >> 2) * (QBUF / 2) + (k & 3) * 32),
+                        umma_desc_sw128(k0 + (k >> 2) * (KV / 2) + (k & 3) * 32), IDESC_QK, k > 0);
+          }
           umma_commit(&kempty[ks]);
           umma_commit(&sfull[buf]);
           if (j == j1 - 1) umma_commit(&qempty[qb]);
@@ -260,6 +369,31 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     // -------------------------------------------------- softmax and epilogue
     const int q = warp & 3;            // TMEM lane quadrant
     const int hf = warp >> 2;          // column half of every row
+    if (FP8 && 32 * q >= G * T) {
+      // ------------------------------------------- FP8: Q quantiser warps
+      // The softmax warps of lane quadrants without rows turn each sequence's
+      // bf16 Q tile into the E4M3 tile the QK UMMA reads, one thread per row,
+      // with a power-of-two scale per row that the softmax applies to the
+      // row's logits.  The row scales have one slot: a sequence's scales are
+      // written only after the softmax warps have read the previous ones.
+      const int ct = ((q - live_quads) * 2 + hf) * 32 + lane, nct = nconv * 32;
+      bool dead = false;
+      int sq = 0;
+      for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+           (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
+           cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
+        const int qb = sq % NQ;
+        if (!dead)
+          dead = __any_sync(0xffffffffu, !mbar_wait(&qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err));
+        if (!dead && sq >= 1)
+          dead = __any_sync(0xffffffffu, !mbar_wait(qsfree, static_cast<uint32_t>(sq - 1) & 1u, p.err));
+        for (int r = ct; r < G * T; r += nct)
+          qscale[r] = quantize_q_row(qbase + qb * QBUF, QBUF / 2, qf8, qf8 + kQf8Tile, r);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qcv[qb]);
+      }
+    } else {
     const int r = 32 * q + lane;
     const int t = r / G, gl = r % G;
     const bool valid = t < T;
@@ -268,13 +402,23 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     float* xmax = ml + 512;            // [2 pages][2 halves][128 rows]
     float* xl = ml + 1024;             // [2 halves][128 rows]
     bool dead = false;
-    int it = 0;
+    int it = 0, sq = 0;
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-         (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup); cursor_next(cur, scan, nitems, Hk, sparse)) {
+         (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
+         cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
       const int L = p.kv_lens[cur.b];
       const int bound = valid ? L - T + t : -1;
       const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
       float m_use = -INFINITY, l = 0.f;
+      // logit scale in the log2 domain; FP8: times the row's Q scale
+      float scale = p.scale_log2;
+      if constexpr (FP8) {
+        if (!dead)
+          dead = __any_sync(0xffffffffu, !mbar_wait(&qcv[sq % NQ], static_cast<uint32_t>(sq / NQ) & 1u, p.err));
+        scale *= valid ? qscale[r] : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qsfree);
+      }
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int buf = it % kSBufs;
         // the page's plan entry is loaded before the wait, so its latency
@@ -301,7 +445,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           float mloc = -INFINITY;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            float v = __uint_as_float(i < 32 ? ra[i] : rb[i - 32]) * p.scale_log2;
+            float v = __uint_as_float(i < 32 ? ra[i] : rb[i - 32]) * scale;
             if (masked && pos0 + hf * 64 + i > bnd) v = -INFINITY;
             x[i] = v;
             mloc = fmaxf(mloc, v);
@@ -335,16 +479,39 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
             tmem_st_wait();
           }
           const bool none = m_use == -INFINITY;
-          uint32_t w[32];
+          if constexpr (FP8) {
+            // P = P_hi + P_lo as E4M3, four positions per TMEM column (P is at
+            // most 2^8 < 448: the reference maximum lags by at most 8); l sums
+            // the fp32 values
+            uint32_t wh[16], wl[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = none ? 0.f : fast_exp2(x[2 * i] - m_use);
-            const float p1 = none ? 0.f : fast_exp2(x[2 * i + 1] - m_use);
-            l += p0 + p1;
-            __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-            w[i] = *reinterpret_cast<uint32_t*>(&pk);
+            for (int i = 0; i < 16; ++i) {
+              float pv[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                pv[k] = none ? 0.f : fast_exp2(x[4 * i + k] - m_use);
+                l += pv[k];
+              }
+              uint32_t h0, l0, h1, l1;
+              split_e4m3x2(__floats2half2_rn(pv[0], pv[1]), h0, l0);
+              split_e4m3x2(__floats2half2_rn(pv[2], pv[3]), h1, l1);
+              wh[i] = (h0 & 0xFFFFu) | (h1 << 16);
+              wl[i] = (l0 & 0xFFFFu) | (l1 << 16);
+            }
+            tmem_st16(tl + buf * 128 + hf * 16, wh);
+            tmem_st16(tl + buf * 128 + 32 + hf * 16, wl);
+          } else {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float p0 = none ? 0.f : fast_exp2(x[2 * i] - m_use);
+              const float p1 = none ? 0.f : fast_exp2(x[2 * i + 1] - m_use);
+              l += p0 + p1;
+              __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+              w[i] = *reinterpret_cast<uint32_t*>(&pk);
+            }
+            tmem_st32(tl + buf * 128 + hf * 32, w);
           }
-          tmem_st32(tl + buf * 128 + hf * 32, w);
           tmem_st_wait();
         }
         // V rows at or past kv_len may hold anything (NaN included): P is zero
@@ -355,9 +522,10 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           if (!dead)
             dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, p.err));
           uint8_t* vst = vring + vs * KV;
-          const int nchunks = (kPage - nvalid) * 16;  // 2 column blocks x 8 chunks per token
+          constexpr int NHALF = FP8 ? 1 : 2;  // 128-byte column blocks per token row
+          const int nchunks = (kPage - nvalid) * 8 * NHALF;
           for (int idx = lane; idx < nchunks; idx += 32) {
-            const int tok = nvalid + idx / 16, part = idx % 16;
+            const int tok = nvalid + idx / (8 * NHALF), part = idx % (8 * NHALF);
             *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
                                       (part & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -425,6 +593,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       }
       tc_fence_before();
     }
+    }  // softmax warps
   }
 
   tc_fence_before();

@@ -28,6 +28,7 @@ constexpr int kMaxCombineParts = 1024;  // upper bound on num_ctas
 constexpr int kUmmaAttnQTiles = 1;
 constexpr int kUmmaAttnKStagesMax = 3;
 constexpr int kUmmaAttnVStages = 3;
+constexpr int kUmmaAttnFp8Stages = 6;  // most FP8 K and V pages (16 KB each) per ring
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
 // stream-K setup charge per sequence, in units (pages or blocks)
 constexpr int kSeqSetup = 3;       // mma.sync attention
@@ -66,6 +67,7 @@ struct AttnParams {
   int off_stage, stage_bytes, off_k, off_v, off_conv, off_merge, off_ml, off_scan, off_bar;
   int off_q, off_vring, nv, nq;  // tcgen05 kernel: Q tiles (nq), V ring (nv); K ring at off_stage, nstages
   int qbuf;                      // tcgen05 kernel: bytes of one Q tile (rows x 256)
+  int off_qf8;                   // tcgen05 kernel, FP8 caches: E4M3 Q tile (rows x 128 B)
   int setup;                     // virtual units charged per sequence start (stream-K weight)
 };
 

@@ -24,6 +24,11 @@ cudaError_t launch_proxy_fp8(int head_dim, int mt, const CUtensorMap& map, const
 cudaError_t launch_attn_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const AttnParams& p,
                              int grid, size_t smem, cudaStream_t st);
 
+// tcgen05 attention over FP8 E4M3 caches: head_dim 128, power-of-two group,
+// group * qo_len <= 64 (kind::f8f6f4 UMMAs; Q and P rounded to E4M3)
+cudaError_t launch_attn_umma_fp8(const CUtensorMap& kv_map, const CUtensorMap& q_map, const AttnParams& p,
+                                 int grid, size_t smem, cudaStream_t st);
+
 // tcgen05 proxy: bf16, head_dim 128, power-of-two group <= 16, group * qo_len <= 128
 cudaError_t launch_proxy_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const ProxyParams& p,
                               int grid, size_t smem, cudaStream_t st);

@@ -177,6 +177,27 @@ def test_dense_stale_pages_hold_nan(Hq, Hk):
     check_dense(p2, num_ctas=2, out_dtype="f32")
 
 
+@pytest.mark.parametrize("Hq,Hk", [(32, 4), (64, 4)])
+def test_dense_fp8_stale_positions_hold_nan(Hq, Hk):
+    """FP8 cache: positions past kv_len inside used pages hold the E4M3 NaN
+    code (0x7F); the output must not see them."""
+    p = W.make_problem(kv_lens=[100, 257, 130, 4], qo_len=4, num_q_heads=Hq, num_kv_heads=Hk,
+                       head_dim=128, kv_dtype=W.FP8, seed=19, slack_slots=3)
+    pool = p.pool.clone()
+    flat = pool.view(torch.uint8).view(-1)
+    for b in range(p.batch):
+        L = int(p.kv_lens[b])
+        for pos in range(L, ((L + 127) // 128) * 128):
+            for h in range(p.num_kv_heads):
+                for kv in (0, 1):
+                    off = oracle.element_offset(int(p.page_table[b, pos // 128]), p.slot_stride,
+                                                p.num_kv_heads, p.head_dim, pos, h, kv, 0)
+                    flat[off:off + p.head_dim] = 0x7F
+    p2 = p.with_(pool=pool)
+    check_dense(p2, out_dtype="f32")
+    check_dense(p2, num_ctas=5, out_dtype="f32")
+
+
 def test_dense_fp8():
     p = W.make_problem(kv_lens=[4096, 300, 129, 1000, 77, 2500], qo_len=4, num_q_heads=32,
                        num_kv_heads=4, head_dim=128, kv_dtype=W.FP8, seed=21, slack_slots=3)
