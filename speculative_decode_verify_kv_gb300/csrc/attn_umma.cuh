@@ -146,13 +146,11 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   const int nitems = sparse ? p.batch * Hk : p.batch;
   int32_t* warp_tot = scan + nitems + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // softmax warps of lane quadrants that hold rows; with FP8 the others convert
-  const int live_quads = (G * T + 31) / 32;
-  const int nsoft = FP8 ? 2 * live_quads : 8;        // arrivals on pfull
-  const int nconv = 8 - 2 * live_quads;              // FP8: warps quantising Q
-
   if (threadIdx.x == 0) {
-    const int ncv = nconv > 0 ? nconv : 1;
+    // softmax warps: all eight, or with FP8 those of lane quadrants holding
+    // rows (the others quantise Q)
+    const int live_quads = (G * T + 31) / 32;
+    const int nsoft = FP8 ? 2 * live_quads : 8;
     for (int i = 0; i < NK; ++i) { mbar_init(&kfull[i], 1); mbar_init(&kempty[i], 1); }
     for (int i = 0; i < NV; ++i) { mbar_init(&vfull[i], 1); mbar_init(&vempty[i], 1); }
     for (int i = 0; i < kSBufs; ++i) {
@@ -163,10 +161,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
-      mbar_init(&qcv[i], ncv);
     }
     mbar_init(mdone, 1);
-    mbar_init(qsfree, nsoft);
+    if constexpr (FP8) {
+      for (int i = 0; i < 2; ++i) mbar_init(&qcv[i], 8 - nsoft);
+      mbar_init(qsfree, nsoft);
+    }
     fence_mbar_init();
   }
   pdl_wait();  // inputs may come from the previous kernel of the stream
@@ -369,13 +369,14 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     // -------------------------------------------------- softmax and epilogue
     const int q = warp & 3;            // TMEM lane quadrant
     const int hf = warp >> 2;          // column half of every row
-    if (FP8 && 32 * q >= G * T) {
+    if (FP8 && 32 * q >= G * T) {  // (a constant false for bf16 caches)
       // ------------------------------------------- FP8: Q quantiser warps
       // The softmax warps of lane quadrants without rows turn each sequence's
       // bf16 Q tile into the E4M3 tile the QK UMMA reads, one thread per row,
       // with a power-of-two scale per row that the softmax applies to the
       // row's logits.  The row scales have one slot: a sequence's scales are
       // written only after the softmax warps have read the previous ones.
+      const int live_quads = (G * T + 31) / 32, nconv = 8 - 2 * live_quads;
       const int ct = ((q - live_quads) * 2 + hf) * 32 + lane, nct = nconv * 32;
       bool dead = false;
       int sq = 0;
