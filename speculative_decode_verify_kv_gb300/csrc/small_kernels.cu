@@ -138,10 +138,15 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int kTopkCachedPages = 1024;  // 32 KB of keys per 8-warp block
+
 __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __restrict__ lens,
                             int batch, int qo_len, int num_kv_heads, int max_pages, int topk,
                             int32_t* __restrict__ out, int* err) {
   __shared__ uint32_t hist_all[8][256];
+  // rows of at most kTopkCachedPages scores keep their order keys in shared
+  // memory for the five passes; longer rows re-read them from global memory
+  extern __shared__ uint32_t keys_all[];  // [8 warps][max_pages] when cached
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,13 +166,20 @@ __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __r
     for (int i = lane; i < topk; i += 32) orow[i] = i < n ? i : -1;
     return;
   }
+  const bool cached = max_pages <= kTopkCachedPages;
+  uint32_t* keys = keys_all + warp * max_pages;
+  if (cached) {
+    for (int i = lane; i < n; i += 32) keys[i] = order_key(srow[i]);
+    __syncwarp();
+  }
+  auto key_at = [&](int i) -> uint32_t { return cached ? keys[i] : order_key(srow[i]); };
   uint32_t prefix = 0, pmask = 0;
   int remaining = topk;  // picks still to place among keys matching the prefix
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
     for (int i = lane; i < n; i += 32) {
-      const uint32_t key = order_key(srow[i]);
+      const uint32_t key = key_at(i);
       if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
     }
     __syncwarp();
@@ -213,7 +225,7 @@ __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __r
   for (int base = 0; base < n; base += 32) {
     const int i = base + lane;
     uint32_t key = 0;
-    if (i < n) key = order_key(srow[i]);
+    if (i < n) key = key_at(i);
     const bool eq = i < n && key == prefix;
     const unsigned eqm = __ballot_sync(0xffffffffu, eq);
     const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
@@ -454,7 +466,8 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
                         cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(batch) * qo_len * num_kv_heads;
   const int blocks = static_cast<int>((rows + 7) / 8);
-  return launch_pdl(topk_kernel, dim3(blocks), dim3(256), 0, st, scores, lens, batch, qo_len, num_kv_heads,
+  const size_t smem = max_pages <= kTopkCachedPages ? static_cast<size_t>(8) * max_pages * sizeof(uint32_t) : 0;
+  return launch_pdl(topk_kernel, dim3(blocks), dim3(256), smem, st, scores, lens, batch, qo_len, num_kv_heads,
                     max_pages, topk, out, err);
 }
 
