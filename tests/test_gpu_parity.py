@@ -251,6 +251,45 @@ def test_dense_bad_page_id_flagged():
     assert T.trtv_get_device_error() & T.DEVERR_PAGE_ID
 
 
+@pytest.mark.parametrize("Hq,Hk", [(32, 4), (64, 4), (16, 2)])   # tcgen05 E4M3: 32 / 64 / 32 rows
+def test_dense_fp8_invalid_requests_and_bad_page(Hq, Hk):
+    """FP8 caches on the tensor-core path: invalid kv_len rows are zero and
+    flagged, a bad page id is flagged, and the valid requests still match."""
+    p = W.make_problem(kv_lens=[300, 200, 100, 700], qo_len=4, num_q_heads=Hq, num_kv_heads=Hk,
+                       head_dim=128, kv_dtype=W.FP8, seed=8, max_pages_per_req=6)
+    lens = p.kv_lens.clone()
+    lens[1] = 2           # shorter than qo_len
+    lens[2] = 1000        # beyond capacity (6 pages)
+    dv = DeviceVerify(p, num_ctas=7, out_dtype="f32")
+    dv.kv_lens.copy_(lens)
+    out = dv.dense().cpu()
+    assert T.trtv_get_device_error() & T.DEVERR_KV_LEN
+    assert torch.all(out[4:12] == 0)
+    ref, bad = oracle.verify_dense(oracle.Inputs(p, kv_lens=lens))
+    assert bad == 2
+    assert np.abs(out.numpy() - ref).max() <= TOL_FP8
+    dv.kv_lens.copy_(p.kv_lens)
+    dv.page_table[3, 1] = p.num_slots + 5
+    dv.dense()
+    assert T.trtv_get_device_error() & T.DEVERR_PAGE_ID
+
+
+def test_sparse_fp8_full_k_equals_dense():
+    """k >= valid blocks on an FP8 cache: the sparse pass equals the dense one
+    (both on the tensor-core E4M3 path, 64 rows)."""
+    p = W.make_problem(kv_lens=[1000, 129, 4, 700], qo_len=4, num_q_heads=64, num_kv_heads=4,
+                       head_dim=128, kv_dtype=W.FP8, seed=44, topk=8, max_pages_per_req=8)
+    dv = DeviceVerify(p, out_dtype="f32")
+    dense = dv.dense().clone()
+    dv.proxy()
+    dv.select()
+    sp = dv.sparse()
+    torch.cuda.synchronize()
+    assert (dense - sp).abs().max().item() < 2e-2
+    ref, _ = oracle.verify_dense(oracle.Inputs(p))
+    assert np.abs(sp.cpu().numpy() - ref).max() <= TOL_FP8
+
+
 @pytest.mark.parametrize("Hq", [32, 64])  # 32 rows (mma.sync), 64 rows (tcgen05)
 def test_dense_graph_replay_with_mutated_lens(Hq):
     """Capture once, then grow and shrink kv_lens on the device between replays
