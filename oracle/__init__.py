@@ -76,6 +76,9 @@ def _bind(h: ctypes.CDLL) -> ctypes.CDLL:
     h.trtvo_e4m3_from_float.restype = ctypes.c_uint8
     h.trtvo_e4m3_from_float.argtypes = [ctypes.c_float]
     h.trtvo_stage_kv.argtypes = [P, vp, vp, vp, vp, vp]
+    h.trtvo_flatten_page_table.argtypes = [P, vp, vp, vp, vp]
+    h.trtvo_page_table_from_flat.argtypes = [P, vp, vp, vp]
+    h.trtvo_draft_attn.argtypes = [P, vp, vp, vp, vp, vp, vp]
     h.trtvo_num_threads.restype = ctypes.c_int
     return h
 
@@ -224,6 +227,38 @@ class Oracle:
         bad = self.h.trtvo_stage_kv(ctypes.byref(P), _ptr(kn), _ptr(vn), _ptr(x.pt), _ptr(x.lens),
                                     _ptr(pool))
         return pool, bad
+
+    def flatten_page_table(self, x: Inputs, flat_init=None):
+        """Flat table [B*max_pages] and indptr [B+1] restaged from the padded
+        table and the lengths; entries past indptr[B] keep ``flat_init``
+        (zeros by default).  Returns (flat, indptr, invalid requests)."""
+        P = x.P
+        n = P.batch * P.max_pages_per_req
+        flat = (np.zeros(n, np.int32) if flat_init is None
+                else np.array(_np(flat_init, np.int32), dtype=np.int32).reshape(-1).copy())
+        indptr = np.zeros(P.batch + 1, np.int32)
+        bad = self.h.trtvo_flatten_page_table(ctypes.byref(P), _ptr(x.pt), _ptr(x.lens), _ptr(flat),
+                                              _ptr(indptr))
+        return flat, indptr, bad
+
+    def page_table_from_flat(self, x: Inputs, flat):
+        """Padded table [B, max_pages] from a flat table whose row bases come
+        from the lengths.  Returns (page_table, invalid requests)."""
+        P = x.P
+        f = _np(flat, np.int32)
+        pt = np.zeros((P.batch, P.max_pages_per_req), np.int32)
+        bad = self.h.trtvo_page_table_from_flat(ctypes.byref(P), _ptr(f), _ptr(x.lens), _ptr(pt))
+        return pt, bad
+
+    def draft_attn(self, x: Inputs, k_sub, v_sub):
+        """Attention through the P32 sub-page tables k_sub / v_sub [B, 4*max_pages]."""
+        P = x.P
+        ks = _np(k_sub, np.int32)
+        vs = _np(v_sub, np.int32)
+        out = np.zeros((P.batch * P.qo_len, P.num_q_heads, P.head_dim), np.float64)
+        bad = self.h.trtvo_draft_attn(ctypes.byref(P), _ptr(x.q), _ptr(x.pool), _ptr(ks), _ptr(vs),
+                                      _ptr(x.lens), _ptr(out))
+        return out, bad
 
     def num_threads(self) -> int:
         return self.h.trtvo_num_threads()

@@ -486,6 +486,143 @@ int trtvo_stage_kv(const trtvo_problem* P, const uint16_t* k_new, const uint16_t
     return bad;
 }
 
+/* ---- f3: flat (CSR) page table rebuilt from the lengths ------------------ */
+
+/* Pages request b occupies in the flat table: ceil(kv_len / 128), taken as 0
+ * for a negative length and as max_pages for a length past the row's
+ * capacity, so that every later row's base stays defined. */
+static int64_t flat_pages_of(const trtvo_problem* P, int32_t L) {
+    if (L <= 0) return 0;
+    int64_t n = ((int64_t)L + TRTVO_PAGE - 1) / TRTVO_PAGE;
+    return n > P->max_pages_per_req ? P->max_pages_per_req : n;
+}
+
+/* Restage the flat table from the padded one and the current lengths
+ * ([PR3], "Overlap-correction fix": a length correction that moves a row
+ * across a page boundary changes the row bases, so the flat table is rebuilt
+ * from the corrected lengths):
+ *   indptr[0] = 0,  indptr[b + 1] = indptr[b] + n_b,
+ *   flat[indptr[b] + j] = page_table[b][j]  for j < n_b.
+ * flat entries at or past indptr[batch] are left as they were; indptr may be
+ * NULL.  Returns the number of requests whose length is outside
+ * [qo_len, 128 * max_pages]. */
+int trtvo_flatten_page_table(const trtvo_problem* P, const int32_t* pt, const int32_t* lens,
+                             int32_t* flat, int32_t* indptr) {
+    int bad = 0;
+    int64_t base = 0;
+    if (indptr) indptr[0] = 0;
+    for (int b = 0; b < P->batch; ++b) {
+        int32_t L = lens[b];
+        if (L < P->qo_len || (int64_t)L > (int64_t)TRTVO_PAGE * P->max_pages_per_req) ++bad;
+        int64_t n = flat_pages_of(P, L);
+        for (int64_t j = 0; j < n; ++j) flat[base + j] = pt[(int64_t)b * P->max_pages_per_req + j];
+        base += n;
+        if (indptr) indptr[b + 1] = (int32_t)base;
+    }
+    return bad;
+}
+
+/* The consumer's side of the same layout: row b of the flat table starts at
+ * sum_{b' < b} n_{b'}, computed from the lengths (the row bases are not an
+ * input), and the padded table is
+ *   page_table[b][j] = flat[base_b + j]  for j < n_b,  0 (slot 0) otherwise
+ * (padded entries address slot 0, [PR18066]).  Returns the number of requests
+ * whose length is outside [qo_len, 128 * max_pages]. */
+int trtvo_page_table_from_flat(const trtvo_problem* P, const int32_t* flat, const int32_t* lens,
+                               int32_t* pt) {
+    int bad = 0;
+    int64_t base = 0;
+    for (int b = 0; b < P->batch; ++b) {
+        int32_t L = lens[b];
+        if (L < P->qo_len || (int64_t)L > (int64_t)TRTVO_PAGE * P->max_pages_per_req) ++bad;
+        int64_t n = flat_pages_of(P, L);
+        for (int64_t j = 0; j < P->max_pages_per_req; ++j)
+            pt[(int64_t)b * P->max_pages_per_req + j] = j < n ? flat[base + j] : 0;
+        base += n;
+    }
+    return bad;
+}
+
+/* ---- f4: drafter attention through the P32 sub-page tables --------------- */
+
+/* Position p of KV head h of request b lives in sub-page k_sub[b][p / 32]
+ * (V: v_sub[b][p / 32]), at element (h * 32 + p % 32) * head_dim + d of that
+ * sub-page; a sub-page is one [kv_heads, 32, head_dim] block and index 0 is
+ * the first sub-page of the view ([PR17835], "Grouped-HND draft KV
+ * transfer"; the view's index scale is the layer-local slot stride,
+ * [PR18066]).  The view spans 4 * num_slots * slot_stride sub-pages. */
+static int draft_request_valid(const trtvo_problem* P, const int32_t* k_sub, const int32_t* v_sub,
+                               const int32_t* lens, int b) {
+    int32_t L = lens[b];
+    int64_t nsub = (int64_t)TRTVO_GROUPS * P->max_pages_per_req;
+    if (L < P->qo_len || (int64_t)L > (int64_t)TRTVO_SUBPAGE * nsub) return 0;
+    int64_t limit = (int64_t)TRTVO_GROUPS * P->num_slots * P->slot_stride;
+    int64_t used = ((int64_t)L + TRTVO_SUBPAGE - 1) / TRTVO_SUBPAGE;
+    for (int64_t j = 0; j < used; ++j) {
+        int64_t ks = k_sub[(int64_t)b * nsub + j], vs = v_sub[(int64_t)b * nsub + j];
+        if (ks < 0 || ks >= limit || vs < 0 || vs >= limit) return 0;
+    }
+    return 1;
+}
+
+static void gather_head_p32(const trtvo_problem* P, const void* pool, const int32_t* k_sub,
+                            const int32_t* v_sub, int b, int L, int h, double* Kc, double* Vc) {
+    int D = P->head_dim;
+    int64_t nsub = (int64_t)TRTVO_GROUPS * P->max_pages_per_req;
+    int64_t sub_elems = (int64_t)P->num_kv_heads * TRTVO_SUBPAGE * D;
+    for (int p = 0; p < L; ++p) {
+        int64_t ks = k_sub[(int64_t)b * nsub + p / TRTVO_SUBPAGE];
+        int64_t vs = v_sub[(int64_t)b * nsub + p / TRTVO_SUBPAGE];
+        int64_t in_sub = ((int64_t)h * TRTVO_SUBPAGE + p % TRTVO_SUBPAGE) * D;
+        for (int d = 0; d < D; ++d) {
+            Kc[(int64_t)p * D + d] = load_kv(P, pool, ks * sub_elems + in_sub + d, 0);
+            Vc[(int64_t)p * D + d] = load_kv(P, pool, vs * sub_elems + in_sub + d, 1);
+        }
+    }
+}
+
+/* out[(b*T + t)][hq][d]: the drafter's attention reads its KV through the P32
+ * tables alone ([PR17835]: the drafter consumes P32 pages of the shared P128
+ * allocation).  Query row (b, t, hq) attends positions p <= kv_len - qo_len + t
+ * of KV head hq / G; qo_len = 1 is the drafter's plain decode step.  Returns
+ * the number of invalid requests (length outside [qo_len, 32 * 4 * max_pages],
+ * or a used sub-page index outside the view); their rows are zero. */
+int trtvo_draft_attn(const trtvo_problem* P, const uint16_t* q, const void* pool,
+                     const int32_t* k_sub, const int32_t* v_sub, const int32_t* lens,
+                     double* out) {
+    int B = P->batch, T = P->qo_len, Hq = P->num_q_heads, Hk = P->num_kv_heads, D = P->head_dim;
+    int G = Hq / Hk;
+    int bad = 0;
+    for (int b = 0; b < B; ++b) bad += !draft_request_valid(P, k_sub, v_sub, lens, b);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * Hk; ++bh) {
+        int b = bh / Hk, h = bh % Hk;
+        if (!draft_request_valid(P, k_sub, v_sub, lens, b)) {
+            for (int t = 0; t < T; ++t)
+                for (int g = 0; g < G; ++g)
+                    memset(out + (((int64_t)b * T + t) * Hq + h * G + g) * D, 0, sizeof(double) * D);
+            continue;
+        }
+        int L = lens[b];
+        double* Kc = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* Vc = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* x = (double*)malloc(sizeof(double) * (size_t)L);
+        double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+        gather_head_p32(P, pool, k_sub, v_sub, b, L, h, Kc, Vc);
+        for (int t = 0; t < T; ++t) {
+            int visible = L - T + t + 1;
+            for (int g = 0; g < G; ++g) {
+                int hq = h * G + g;
+                load_q(P, q, b, t, hq, qv);
+                attend_row(P, qv, Kc, Vc, visible, NULL, x,
+                           out + (((int64_t)b * T + t) * Hq + hq) * D);
+            }
+        }
+        free(Kc); free(Vc); free(x); free(qv);
+    }
+    return bad;
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int trtvo_num_threads(void) {
 #ifdef _OPENMP

@@ -585,4 +585,171 @@ def check_stage_kv_skips_invalid_requests(orc):
                 assert not changed[pt_np[b, j] * 2 + kv].any(), (b, kv)
 
 
+
+# ---------------------------------------------------------------------------
+# flat (CSR) page table rebuilt from the lengths
+
+def _flat_golden():
+    rows = _rows("flat_page_table.txt")
+    g = {"pt": {}, "table": {}, "stale_table": {}}
+    for r in rows:
+        if r[0] in g:
+            g[r[0]][int(r[1])] = [int(v) for v in r[2:]]
+        else:
+            g[r[0]] = [int(v) for v in r[1:]]
+    B = len(g["pt"])
+    pt = np.array([g["pt"][b] for b in range(B)], np.int32)
+    return g, B, pt
+
+
+def check_flat_page_table_golden(orc):
+    g, B, pt = _flat_golden()
+    p = small(lens=g["lens"], T=g["qo_len"][0])
+    assert p.max_pages_per_req == g["max_pages"][0]
+    x = O.Inputs(p, page_table=torch.from_numpy(pt))
+    flat, indptr, bad = orc.flatten_page_table(x)
+    n = g["indptr"][-1]
+    assert bad == 0
+    assert list(indptr) == g["indptr"]
+    assert list(flat[:n]) == g["flat"]
+    table, bad = orc.page_table_from_flat(x, flat)
+    assert bad == 0
+    assert table.tolist() == [g["table"][b] for b in range(B)]
+    # the correction: restaged from the corrected lengths
+    xc = O.Inputs(p, page_table=torch.from_numpy(pt),
+                  kv_lens=torch.tensor(g["lens_corrected"], dtype=torch.int32))
+    flat_c, indptr_c, _ = orc.flatten_page_table(xc)
+    assert list(indptr_c) == g["indptr_corrected"]
+    assert list(flat_c[:indptr_c[-1]]) == g["flat_corrected"]
+    # the stale flat table read with the corrected lengths misbases rows 2, 3
+    stale, _ = orc.page_table_from_flat(xc, flat)
+    assert stale.tolist() == [g["stale_table"][b] for b in range(B)]
+
+
+def check_flat_roundtrip_keeps_verify(orc):
+    """flatten -> rebuild returns the used part of the padded table (padding
+    -> slot 0), entries past the last row are untouched, and the verify
+    output on the rebuilt table is the output on the original."""
+    p = small(seed=41, lens=(5, 130, 300, 1, 256), stride=2)
+    pt = p.page_table.clone()
+    pt[0, 1:] = 7                 # garbage past request 0's used page
+    pt[3, :] = 1                  # kv_len 1 < qo_len: invalid, still one page in the layout
+    x = O.Inputs(p, page_table=pt)
+    sentinel = np.full(p.batch * p.max_pages_per_req, -77, np.int32)
+    flat, indptr, bad = orc.flatten_page_table(x, flat_init=sentinel)
+    assert bad == 1
+    used = [(int(L) + 127) // 128 for L in p.kv_lens]
+    assert list(np.diff(indptr)) == used
+    assert np.all(flat[indptr[-1]:] == -77)
+    table, _ = orc.page_table_from_flat(x, flat)
+    ptn = pt.numpy()
+    for b, n in enumerate(used):
+        assert list(table[b, :n]) == list(ptn[b, :n])
+        assert np.all(table[b, n:] == 0)
+    o1, _ = orc.verify_dense(x)
+    o2, _ = orc.verify_dense(O.Inputs(p, page_table=torch.from_numpy(table)))
+    assert np.array_equal(o1, o2)
+
+
+def check_flat_shrink_across_page_boundary(orc):
+    """A length correction across a page boundary: the restaged flat table
+    gives the attention of the corrected problem (checked against torch SDPA
+    over contiguous K/V read by the numpy layout); the stale one moves the
+    later rows onto other pages."""
+    T = 2
+    p = small(seed=43, lens=(300, 257, 200, 140), T=T, stride=2)
+    lens_c = torch.tensor([300, 255, 200, 140], dtype=torch.int32)   # 3 pages -> 2
+    xc = O.Inputs(p, kv_lens=lens_c)
+    flat_old, _, _ = orc.flatten_page_table(O.Inputs(p))
+    flat_new, _, _ = orc.flatten_page_table(xc)
+    good, _ = orc.page_table_from_flat(xc, flat_new)
+    stale, _ = orc.page_table_from_flat(xc, flat_old)
+    out, bad = orc.verify_dense(O.Inputs(p, kv_lens=lens_c, page_table=torch.from_numpy(good)))
+    assert bad == 0
+    pool5 = pool5_of(p)
+    q = q64(p)
+    G = p.num_q_heads // p.num_kv_heads
+    ptn = p.page_table.numpy()
+    for b in range(p.batch):
+        L = int(lens_c[b])
+        K = decoded(p, gather_contiguous(pool5, ptn, 2, b, L, 0), 0)
+        V = decoded(p, gather_contiguous(pool5, ptn, 2, b, L, 1), 1)
+        for t in range(T):
+            n = L - T + t + 1
+            for hq in range(p.num_q_heads):
+                want = sdpa(q[b * T + t, hq], K[:n, hq // G], V[:n, hq // G], p.sm_scale)
+                assert np.allclose(out[b * T + t, hq], want, atol=1e-12, rtol=1e-12), (b, t, hq)
+    assert np.array_equal(stale[:2], good[:2])
+    assert not np.array_equal(stale[2:], good[2:])
+
+
+# ---------------------------------------------------------------------------
+# drafter attention through the P32 sub-page tables
+
+def check_draft_attn_via_view_equals_dense(orc):
+    """The P32 tables of the sub-page view address the bytes the P128 table
+    does: attention through them equals the dense verify, for T = 1 and a
+    ladder, bf16 and FP8, stride 2 and a layer-local stride of 8."""
+    for T, dtype, stride in ((1, W.BF16, 2), (3, W.FP8, 8), (1, W.FP8, 8)):
+        p = small(seed=47 + T, lens=(33, 130, 300), T=T, stride=stride, kv_dtype=dtype)
+        x = O.Inputs(p)
+        k_sub, v_sub, _ = orc.subpage_view(x)
+        want, bad0 = orc.verify_dense(x)
+        got, bad = orc.draft_attn(x, k_sub, v_sub)
+        assert bad == bad0 == 0
+        assert np.array_equal(got, want), (T, dtype, stride)
+
+
+def check_draft_attn_shuffled_subpages_vs_sdpa(orc):
+    """Decode (qo_len 1) through P32 tables whose sub-pages are an arbitrary
+    permutation of the pool's sub-pages (not grouped four to a page): the
+    output is SDPA over K/V rows gathered by numpy from the [sub-page, head,
+    32, D] view of the pool."""
+    p = small(seed=53, lens=(70, 31, 160), T=1, Hq=8, Hk=2, D=32, stride=3)
+    nsub_pool = 4 * p.num_slots * p.slot_stride
+    nsub = 4 * p.max_pages_per_req
+    gen = np.random.default_rng(53)
+    k_sub = gen.permutation(nsub_pool)[:p.batch * nsub].reshape(p.batch, nsub).astype(np.int32)
+    v_sub = gen.permutation(nsub_pool)[:p.batch * nsub].reshape(p.batch, nsub).astype(np.int32)
+    x = O.Inputs(p)
+    got, bad = orc.draft_attn(x, k_sub, v_sub)
+    assert bad == 0
+    subs = pool5_of(p).reshape(nsub_pool, p.num_kv_heads, 32, p.head_dim)
+    q = q64(p)
+    G = p.num_q_heads // p.num_kv_heads
+    for b in range(p.batch):
+        L = int(p.kv_lens[b])
+        for hq in range(p.num_q_heads):
+            h = hq // G
+            Kr = np.stack([subs[k_sub[b, i // 32], h, i % 32] for i in range(L)])
+            Vr = np.stack([subs[v_sub[b, i // 32], h, i % 32] for i in range(L)])
+            want = sdpa(q[b, hq], decoded(p, Kr, 0), decoded(p, Vr, 1), p.sm_scale)
+            assert np.allclose(got[b, hq], want, atol=1e-12, rtol=1e-12), (b, hq)
+
+
+def check_draft_attn_layer_stride_and_invalid(orc):
+    """A pool whose slots hold eight buffers (this layer's K and V plus six of
+    other layers, here NaN): the view built with the layer-local stride reads
+    none of the others.  A used sub-page index outside the view makes the
+    request invalid (zero rows); an unused one does not."""
+    p = small(seed=59, lens=(40, 129, 250), T=2, stride=8)
+    pool = p.pool.clone()
+    pool.view(p.num_slots, 8, -1)[:, 2:] = float("nan")
+    x = O.Inputs(p, pool=pool)
+    k_sub, v_sub, _ = orc.subpage_view(x)
+    got, bad = orc.draft_attn(x, k_sub, v_sub)
+    assert bad == 0 and np.all(np.isfinite(got))
+    want, _ = orc.verify_dense(x)
+    assert np.array_equal(got, want)
+    limit = 4 * p.num_slots * 8
+    k_bad = k_sub.copy()
+    k_bad[1, 4] = limit                 # sub-page 4 of request 1 (positions 128..159) is used
+    k_bad[0, 5] = limit                 # request 0 uses sub-pages 0..1 only
+    got2, bad2 = orc.draft_attn(x, k_bad, v_sub)
+    assert bad2 == 1
+    T, Hq = p.qo_len, p.num_q_heads
+    assert np.all(got2[T:2 * T] == 0)
+    assert np.array_equal(got2[:T], got[:T]) and np.array_equal(got2[2 * T:], got[2 * T:])
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

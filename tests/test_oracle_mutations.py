@@ -37,6 +37,15 @@ MUTATIONS = [
                                "const float scale = (float)(kv == 0 ? P->v_scale : P->k_scale);")]),
     ("e4m3_ties_to_lower", [("if (err < best_err || (err == best_err && (c & 1) == 0)) {", "if (err < best_err) {")]),
     ("e4m3_no_saturation", [("for (int c = 0; c < 0x7F; ++c) {", "if (ax > 448.0) return 0x7F; for (int c = 0; c < 0x7F; ++c) {")]),
+    ("flat_floor_pages", [("int64_t n = ((int64_t)L + TRTVO_PAGE - 1) / TRTVO_PAGE;", "int64_t n = (int64_t)L / TRTVO_PAGE;")]),
+    ("flat_padding_keeps_entry", [("j < n ? flat[base + j] : 0;", "j < n ? flat[base + j] : flat[base];")]),
+    ("flat_rows_at_capacity", [("base += n;", "base += P->max_pages_per_req;")]),
+    ("draft_k_from_v_table", [("int64_t ks = k_sub[(int64_t)b * nsub + p / TRTVO_SUBPAGE];",
+                               "int64_t ks = v_sub[(int64_t)b * nsub + p / TRTVO_SUBPAGE];")]),
+    ("draft_token_rotated", [("int64_t in_sub = ((int64_t)h * TRTVO_SUBPAGE + p % TRTVO_SUBPAGE) * D;",
+                              "int64_t in_sub = ((int64_t)h * TRTVO_SUBPAGE + (p + 1) % TRTVO_SUBPAGE) * D;")]),
+    ("draft_view_without_stride", [("int64_t limit = (int64_t)TRTVO_GROUPS * P->num_slots * P->slot_stride;",
+                                    "int64_t limit = (int64_t)TRTVO_GROUPS * P->num_slots;")]),
 ]
 
 
