@@ -230,6 +230,78 @@ trtv_status trtv_stage_kv(const trtv_geom* geom, const void* k_new, const void* 
                           const int32_t* page_table, const int32_t* kv_lens, void* stream);
 
 /*
+ * Flat (CSR) page table restaged from the padded one and the current lengths
+ * (source: PR #3 "... verify" commit, "Overlap-correction fix": the flat
+ * table's row layout follows the lengths, so a correction that moves a row
+ * across a page boundary moves every later row and the flat table must be
+ * rebuilt from the corrected lengths).  With n_b = ceil(kv_len[b] / 128)
+ * (0 for kv_len <= 0, max_pages_per_req for a longer row):
+ *   indptr[0] = 0,  indptr[b + 1] = indptr[b] + n_b,
+ *   flat[indptr[b] + j] = page_table[b][j]  for j < n_b.
+ *   page_table int32 [batch, max_pages_per_req] (read)
+ *   kv_lens    int32 [batch] (read on the device)
+ *   flat       int32 [batch * max_pages_per_req] (written up to indptr[batch];
+ *              the rest is left as it was)
+ *   indptr     int32 [batch + 1] (written), or NULL
+ * Lengths outside [qo_len, 128 * max_pages_per_req] set TRTV_DEVERR_KV_LEN;
+ * their rows still take n_b entries as above.  batch <= 65536.
+ */
+trtv_status trtv_flatten_page_table(const trtv_geom* geom, const int32_t* page_table,
+                                    const int32_t* kv_lens, int32_t* flat, int32_t* indptr,
+                                    void* stream);
+
+/*
+ * The consumer's side of the flat table: the padded table rebuilt on the
+ * device, the row bases derived from the lengths (not an input), as above:
+ *   page_table[b][j] = flat[indptr[b] + j] for j < n_b, else 0 (padding
+ *   addresses slot 0, #18066 copy_batch_block_offsets commit).
+ *   flat       int32, at least indptr[batch] entries (read)
+ *   kv_lens    int32 [batch] (read on the device)
+ *   page_table int32 [batch, max_pages_per_req] (written, every entry)
+ * Errors as trtv_flatten_page_table.
+ */
+trtv_status trtv_page_table_from_flat(const trtv_geom* geom, const int32_t* flat,
+                                      const int32_t* kv_lens, int32_t* page_table, void* stream);
+
+/*
+ * Dense ladder verify taking the flat table: trtv_page_table_from_flat into
+ * the workspace, then trtv_verify_dense on it (two kernels, same stream).
+ * Workspace: trtv_workspace_bytes(geom, 0) plus
+ * 4 * batch * max_pages_per_req bytes rounded up to 256
+ * (trtv_workspace_bytes_flat).
+ */
+size_t trtv_workspace_bytes_flat(const trtv_geom* geom);
+trtv_status trtv_verify_dense_flat(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                   const int32_t* flat, const int32_t* kv_lens, void* out,
+                                   int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                   void* stream);
+
+/*
+ * Drafter attention through the P32 sub-page tables (sources: #17835: the
+ * Eagle3 drafter consumes P32 pages of the shared P128 allocation through the
+ * non-owning view; #18066 MiniMaxM3DraftKVCacheView commit: the view's index
+ * scale is the draft layer's own slot stride, which may differ from a
+ * pool-level page scale, e.g. 8 against 171).
+ * As trtv_verify_dense (qo_len = 1 is the drafter's decode step; larger
+ * qo_len applies the ladder), except that position p of KV head h of
+ * request b is read from sub-page k_sub[b][p / 32] (V: v_sub[b][p / 32]) of
+ * the view, element (h * 32 + p % 32) * head_dim + d of that sub-page, the
+ * view's sub-page 0 being the pool's first [num_kv_heads, 32, head_dim]
+ * block.  page_table is not an input: the tables may come from
+ * trtv_subpage_view or from any other producer, in any order.
+ *   k_sub, v_sub int32 [batch, 4 * max_pages_per_req] (read on the device);
+ *                entries at or past ceil(kv_len / 32) are neither read nor
+ *                checked.
+ * The view spans 4 * num_slots * slot_stride sub-pages; a used entry outside
+ * it sets TRTV_DEVERR_PAGE_ID and sub-page 0 is read instead (finite but
+ * meaningless rows).  Workspace and other errors as trtv_verify_dense.
+ */
+trtv_status trtv_draft_attn_p32(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                const int32_t* k_sub, const int32_t* v_sub, const int32_t* kv_lens,
+                                void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                void* stream);
+
+/*
  * Read and clear the current device's error word (TRTV_DEVERR_* bits).
  * Synchronises `stream`; not for use while capturing a graph.
  */

@@ -19,8 +19,9 @@ __all__ = [
     "TRTV_OK", "TRTV_BF16", "TRTV_FP8_E4M3", "TRTV_F32", "TrtvError", "Geom", "load",
     "trtv_subpage_view", "trtv_workspace_bytes", "trtv_verify_dense", "trtv_msa_proxy_score",
     "trtv_msa_topk", "trtv_msa_sparse_attn", "trtv_get_device_error", "trtv_version",
-    "trtv_verify_dense_noalloc", "trtv_stage_kv",
-    "trtv_status_string", "geom_of", "EXPORTS",
+    "trtv_verify_dense_noalloc", "trtv_stage_kv", "trtv_flatten_page_table",
+    "trtv_page_table_from_flat", "trtv_workspace_bytes_flat", "trtv_verify_dense_flat",
+    "trtv_draft_attn_p32", "trtv_status_string", "geom_of", "EXPORTS",
 ]
 
 TRTV_OK, TRTV_ERR_INVALID_ARG, TRTV_ERR_UNSUPPORTED, TRTV_ERR_CUDA, TRTV_ERR_WORKSPACE = range(5)
@@ -30,7 +31,9 @@ DEVERR_KV_LEN, DEVERR_PAGE_ID, DEVERR_BLOCK_IDX, DEVERR_TIMEOUT = 1, 2, 4, 8
 # every function the C header declares
 EXPORTS = ("trtv_status_string", "trtv_version", "trtv_subpage_view", "trtv_workspace_bytes",
            "trtv_verify_dense", "trtv_verify_dense_noalloc", "trtv_msa_proxy_score", "trtv_msa_topk",
-           "trtv_msa_sparse_attn", "trtv_stage_kv", "trtv_get_device_error")
+           "trtv_msa_sparse_attn", "trtv_stage_kv", "trtv_flatten_page_table",
+           "trtv_page_table_from_flat", "trtv_workspace_bytes_flat", "trtv_verify_dense_flat",
+           "trtv_draft_attn_p32", "trtv_get_device_error")
 
 
 class TrtvError(RuntimeError):
@@ -91,6 +94,16 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     h.trtv_msa_sparse_attn.argtypes = [G, vp, vp, vp, vp, vp, i32, vp, i32, vp, sz, vp]
     h.trtv_stage_kv.restype = ctypes.c_int
     h.trtv_stage_kv.argtypes = [G, vp, vp, vp, vp, vp, vp]
+    h.trtv_flatten_page_table.restype = ctypes.c_int
+    h.trtv_flatten_page_table.argtypes = [G, vp, vp, vp, vp, vp]
+    h.trtv_page_table_from_flat.restype = ctypes.c_int
+    h.trtv_page_table_from_flat.argtypes = [G, vp, vp, vp, vp]
+    h.trtv_workspace_bytes_flat.restype = sz
+    h.trtv_workspace_bytes_flat.argtypes = [G]
+    h.trtv_verify_dense_flat.restype = ctypes.c_int
+    h.trtv_verify_dense_flat.argtypes = [G, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+    h.trtv_draft_attn_p32.restype = ctypes.c_int
+    h.trtv_draft_attn_p32.argtypes = [G, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
     h.trtv_get_device_error.restype = ctypes.c_int
     h.trtv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
     _lib = h
@@ -191,6 +204,38 @@ def trtv_stage_kv(geom: Geom, k_new, v_new, kv_pool, page_table, kv_lens, stream
     _check("trtv_stage_kv", load().trtv_stage_kv(
         ctypes.byref(geom), _ptr(k_new), _ptr(v_new), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens),
         _stream(stream)))
+
+
+def trtv_flatten_page_table(geom: Geom, page_table, kv_lens, flat, indptr=None, stream=None) -> None:
+    """Restage the flat (CSR) page table from the padded one and the lengths."""
+    _check("trtv_flatten_page_table", load().trtv_flatten_page_table(
+        ctypes.byref(geom), _ptr(page_table), _ptr(kv_lens), _ptr(flat), _ptr(indptr),
+        _stream(stream)))
+
+
+def trtv_page_table_from_flat(geom: Geom, flat, kv_lens, page_table, stream=None) -> None:
+    """Padded page table from a flat one whose row bases follow the lengths."""
+    _check("trtv_page_table_from_flat", load().trtv_page_table_from_flat(
+        ctypes.byref(geom), _ptr(flat), _ptr(kv_lens), _ptr(page_table), _stream(stream)))
+
+
+def trtv_workspace_bytes_flat(geom: Geom) -> int:
+    return load().trtv_workspace_bytes_flat(ctypes.byref(geom))
+
+
+def trtv_verify_dense_flat(geom: Geom, q, kv_pool, flat, kv_lens, out, out_dtype: int, workspace,
+                           ws_bytes: int, stream=None) -> None:
+    _check("trtv_verify_dense_flat", load().trtv_verify_dense_flat(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(flat), _ptr(kv_lens), _ptr(out), out_dtype,
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_draft_attn_p32(geom: Geom, q, kv_pool, k_sub, v_sub, kv_lens, out, out_dtype: int,
+                        workspace, ws_bytes: int, stream=None) -> None:
+    """Attention read through the P32 sub-page tables (the drafter's view)."""
+    _check("trtv_draft_attn_p32", load().trtv_draft_attn_p32(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(k_sub), _ptr(v_sub), _ptr(kv_lens),
+        _ptr(out), out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def trtv_get_device_error(stream=None) -> int:

@@ -348,20 +348,43 @@ bool plan_proxy_smem(const trtv_geom* g, const Plan& pl, ProxyParams* a, size_t*
   return *bytes <= kSmemOptin - 1024;
 }
 
-trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, const int32_t* pt,
+// How the attention kernels find a request's pages: a padded P128 table, a
+// flat table rebuilt into the workspace first, or the P32 sub-page tables.
+struct KvIndex {
+  const int32_t* page_table;
+  const int32_t* flat;
+  const int32_t* k_sub;
+  const int32_t* v_sub;
+};
+
+size_t flat_table_bytes(const trtv_geom* g) {
+  return align_up(static_cast<size_t>(g->batch) * g->max_pages_per_req * sizeof(int32_t), 256);
+}
+
+bool flat_geometry_ok(const trtv_geom* g) {
+  return static_cast<int64_t>(g->batch) * g->max_pages_per_req < (int64_t{1} << 31) &&
+         g->batch <= 65536;
+}
+
+trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, const KvIndex& kvi,
                         const int32_t* lens, const int32_t* block_idx, int topk, void* out,
                         int32_t out_dtype, void* ws, size_t ws_bytes, void* stream) {
   const bool sparse = block_idx != nullptr;
+  const bool p32 = kvi.k_sub != nullptr || kvi.v_sub != nullptr;
   Plan pl;
   trtv_status s = make_plan(g, sparse ? topk : 0, &pl);
   if (s != TRTV_OK) return s;
   if (sparse && topk < 1) return TRTV_ERR_INVALID_ARG;
-  if (q == nullptr || pool == nullptr || pt == nullptr || lens == nullptr || out == nullptr)
+  const int32_t* pt = kvi.flat != nullptr ? kvi.flat : kvi.page_table;
+  if (p32 ? (kvi.k_sub == nullptr || kvi.v_sub == nullptr) : pt == nullptr) return TRTV_ERR_INVALID_ARG;
+  if (q == nullptr || pool == nullptr || lens == nullptr || out == nullptr)
     return TRTV_ERR_INVALID_ARG;
   if (out_dtype != TRTV_BF16 && out_dtype != TRTV_F32) return TRTV_ERR_INVALID_ARG;
   if (!aligned(pool, 16) || !aligned(q, 8) || !aligned(out, out_dtype == TRTV_F32 ? 16 : 8))
     return TRTV_ERR_INVALID_ARG;
-  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < pl.ws_total) return TRTV_ERR_WORKSPACE;
+  if (kvi.flat != nullptr && !flat_geometry_ok(g)) return TRTV_ERR_UNSUPPORTED;
+  const size_t ws_need = pl.ws_total + (kvi.flat != nullptr ? flat_table_bytes(g) : 0);
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < ws_need) return TRTV_ERR_WORKSPACE;
   if (sparse && g->max_pages_per_req > 16384) return TRTV_ERR_UNSUPPORTED;
   int* err = err_word();
   if (err == nullptr) return TRTV_ERR_CUDA;
@@ -376,7 +399,12 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   a.q = static_cast<const __nv_bfloat16*>(q);
-  a.page_table = pt;
+  // the flat table's padded form goes to the workspace after the call's own regions
+  int32_t* rebuilt = kvi.flat != nullptr ? reinterpret_cast<int32_t*>(wsb + pl.ws_total) : nullptr;
+  a.page_table = p32 ? nullptr : (rebuilt != nullptr ? rebuilt : kvi.page_table);
+  a.sub_k = kvi.k_sub;
+  a.sub_v = kvi.v_sub;
+  a.num_subpages = static_cast<int>(static_cast<int64_t>(g->num_slots) * g->slot_stride * kGroups);
   a.kv_lens = lens;
   a.out = out;
   a.ws_o = reinterpret_cast<float*>(wsb + pl.ws_o);
@@ -408,6 +436,11 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   // each kernel relative to one page of K and V
   a.setup = umma ? kUmmaSeqSetup : kSeqSetup;
   cudaError_t e;
+  if (rebuilt != nullptr) {
+    e = launch_flat_table(false, kvi.flat, lens, g->batch, g->qo_len, g->max_pages_per_req, rebuilt,
+                          nullptr, err, st);
+    if (e != cudaSuccess) return TRTV_ERR_CUDA;
+  }
   if (sparse) {
     e = launch_sparse_plan(block_idx, lens, g->batch, g->qo_len, g->num_kv_heads,
                            g->max_pages_per_req, topk, pl.plan_cap,
@@ -493,8 +526,8 @@ trtv_status trtv_subpage_view(const trtv_geom* g, const int32_t* page_table, con
 trtv_status trtv_verify_dense(const trtv_geom* geom, const void* q, const void* kv_pool,
                               const int32_t* page_table, const int32_t* kv_lens, void* out,
                               int32_t out_dtype, void* workspace, size_t ws_bytes, void* stream) {
-  return attn_common(geom, q, kv_pool, page_table, kv_lens, nullptr, 0, out, out_dtype, workspace,
-                     ws_bytes, stream);
+  return attn_common(geom, q, kv_pool, KvIndex{page_table, nullptr, nullptr, nullptr}, kv_lens, nullptr,
+                     0, out, out_dtype, workspace, ws_bytes, stream);
 }
 
 trtv_status trtv_verify_dense_noalloc(const trtv_geom* geom, const void* q, const void* kv_pool,
@@ -509,8 +542,8 @@ trtv_status trtv_verify_dense_noalloc(const trtv_geom* geom, const void* q, cons
   if (pl.ws_total > kNoAllocScratchBytes) return TRTV_ERR_WORKSPACE;  // geometry too large
   uint8_t* ws = noalloc_scratch();
   if (ws == nullptr) return TRTV_ERR_CUDA;
-  return attn_common(geom, q, kv_pool, page_table, kv_lens, nullptr, 0, out, out_dtype, ws,
-                     kNoAllocScratchBytes, stream);
+  return attn_common(geom, q, kv_pool, KvIndex{page_table, nullptr, nullptr, nullptr}, kv_lens, nullptr,
+                     0, out, out_dtype, ws, kNoAllocScratchBytes, stream);
 }
 
 trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const void* kv_pool,
@@ -519,8 +552,8 @@ trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const voi
                                  int32_t out_dtype, void* workspace, size_t ws_bytes,
                                  void* stream) {
   if (block_idx == nullptr) return TRTV_ERR_INVALID_ARG;
-  return attn_common(geom, q, kv_pool, page_table, kv_lens, block_idx, topk, out, out_dtype,
-                     workspace, ws_bytes, stream);
+  return attn_common(geom, q, kv_pool, KvIndex{page_table, nullptr, nullptr, nullptr}, kv_lens,
+                     block_idx, topk, out, out_dtype, workspace, ws_bytes, stream);
 }
 
 trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* kv_pool,
@@ -604,6 +637,55 @@ trtv_status trtv_stage_kv(const trtv_geom* g, const void* k_new, const void* v_n
                                         g->slot_stride, g->kv_dtype == TRTV_FP8_E4M3, g->k_scale,
                                         g->v_scale, err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+
+namespace {
+trtv_status flat_table_call(bool to_flat, const trtv_geom* g, const int32_t* src, const int32_t* lens,
+                            int32_t* dst, int32_t* indptr, void* stream) {
+  if (g == nullptr || src == nullptr || lens == nullptr || dst == nullptr) return TRTV_ERR_INVALID_ARG;
+  if (g->batch < 1 || g->qo_len < 1 || g->max_pages_per_req < 1) return TRTV_ERR_INVALID_ARG;
+  if (!flat_geometry_ok(g)) return TRTV_ERR_UNSUPPORTED;
+  int* err = err_word();
+  if (err == nullptr) return TRTV_ERR_CUDA;
+  const cudaError_t e = launch_flat_table(to_flat, src, lens, g->batch, g->qo_len, g->max_pages_per_req,
+                                          dst, indptr, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+}  // namespace
+
+trtv_status trtv_flatten_page_table(const trtv_geom* g, const int32_t* page_table,
+                                    const int32_t* kv_lens, int32_t* flat, int32_t* indptr,
+                                    void* stream) {
+  return flat_table_call(true, g, page_table, kv_lens, flat, indptr, stream);
+}
+
+trtv_status trtv_page_table_from_flat(const trtv_geom* g, const int32_t* flat, const int32_t* kv_lens,
+                                      int32_t* page_table, void* stream) {
+  return flat_table_call(false, g, flat, kv_lens, page_table, nullptr, stream);
+}
+
+size_t trtv_workspace_bytes_flat(const trtv_geom* geom) {
+  Plan pl;
+  if (make_plan(geom, 0, &pl) != TRTV_OK || !flat_geometry_ok(geom)) return 0;
+  return pl.ws_total + flat_table_bytes(geom);
+}
+
+trtv_status trtv_verify_dense_flat(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                   const int32_t* flat, const int32_t* kv_lens, void* out,
+                                   int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  if (flat == nullptr) return TRTV_ERR_INVALID_ARG;
+  return attn_common(geom, q, kv_pool, KvIndex{nullptr, flat, nullptr, nullptr}, kv_lens, nullptr, 0,
+                     out, out_dtype, workspace, ws_bytes, stream);
+}
+
+trtv_status trtv_draft_attn_p32(const trtv_geom* geom, const void* q, const void* kv_pool,
+                                const int32_t* k_sub, const int32_t* v_sub, const int32_t* kv_lens,
+                                void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  if (k_sub == nullptr || v_sub == nullptr) return TRTV_ERR_INVALID_ARG;
+  return attn_common(geom, q, kv_pool, KvIndex{nullptr, nullptr, k_sub, v_sub}, kv_lens, nullptr, 0,
+                     out, out_dtype, workspace, ws_bytes, stream);
 }
 
 trtv_status trtv_get_device_error(int32_t* host_out, void* stream) {

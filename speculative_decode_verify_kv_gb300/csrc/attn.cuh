@@ -285,16 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
          alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
          cursor_next(cur, scan, nitems, Hk, sparse)) {
       const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
+      const int L = p.sub_k != nullptr ? p.kv_lens[cur.b] : 0;  // P32 tables: used entries
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int st = it % NST;
         const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
         if (it >= NST && !mbar_wait(&empty[st], ph ^ 1u, p.err)) { alive = false; break; }
         const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
                                : static_cast<int>(j);
-        int slot = p.page_table[static_cast<int64_t>(cur.b) * p.max_pages + blk];
-        if (slot < 0 || slot >= p.num_slots) {
-          atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
-          slot = 0;
+        const int64_t row = static_cast<int64_t>(cur.b) * p.max_pages + blk;
+        int slot = 0;
+        if (p.sub_k == nullptr) {
+          slot = p.page_table[row];
+          if (slot < 0 || slot >= p.num_slots) {
+            atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
+            slot = 0;
+          }
         }
         uint8_t* stage = smem + p.off_stage + st * p.stage_bytes;
         mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(p.stage_bytes));
@@ -304,7 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = stage + (kv ? p.off_v : p.off_k);
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
-            const int y = static_cast<int>(((kbuf + kv) * kGroups + g) * sub_rows + cur.h * kSub);
+            const int sp = p.sub_k != nullptr
+                               ? p32_entry(kv ? p.sub_v : p.sub_k, row * kGroups + g, blk * kGroups + g,
+                                           L, p.num_subpages, p.err)
+                               : static_cast<int>((kbuf + kv) * kGroups + g);
+            const int y = sp * sub_rows + cur.h * kSub;
 #pragma unroll
             for (int hb = 0; hb < NB; ++hb)
               tma_load_2d(dst + (g * NB + hb) * kBox, &kv_map, &full[st], hb * (FP8 ? 128 : 64), y,

@@ -244,13 +244,18 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
                 : "memory");
         }
         const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
+        const int L = p.sub_k != nullptr ? p.kv_lens[cur.b] : 0;  // P32 tables: used entries
         for (int64_t j = j0; j < j1; ++j, ++it) {
           const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
                                  : static_cast<int>(j);
-          int slot = p.page_table[static_cast<int64_t>(cur.b) * p.max_pages + blk];
-          if (slot < 0 || slot >= p.num_slots) {
-            if (!is_v) atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
-            slot = 0;
+          const int64_t row = static_cast<int64_t>(cur.b) * p.max_pages + blk;
+          int slot = 0;
+          if (p.sub_k == nullptr) {
+            slot = p.page_table[row];
+            if (slot < 0 || slot >= p.num_slots) {
+              if (!is_v) atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
+              slot = 0;
+            }
           }
           const int64_t buf = static_cast<int64_t>(slot) * p.slot_stride + (is_v ? 1 : 0);
           const int st = it % n;
@@ -266,8 +271,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           for (int hb = 0; hb < (FP8 ? 1 : 2); ++hb)
 #pragma unroll
             for (int g = 0; g < kGroups; ++g) {
-              const int y = static_cast<int>((buf * kGroups + g) * sub_rows + cur.h * kSub);
-              tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, &fullb[st], hb * 64, y, pol);
+              const int sp = p.sub_k != nullptr
+                                 ? p32_entry(is_v ? p.sub_v : p.sub_k, row * kGroups + g,
+                                             blk * kGroups + g, L, p.num_subpages, p.err)
+                                 : static_cast<int>(buf * kGroups + g);
+              tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, &fullb[st], hb * 64,
+                          sp * sub_rows + cur.h * kSub, pol);
             }
         }
       }

@@ -69,6 +69,12 @@ struct AttnParams {
   int qbuf;                      // tcgen05 kernel: bytes of one Q tile (rows x 256)
   int off_qf8;                   // tcgen05 kernel, FP8 caches: E4M3 Q tile (rows x 128 B)
   int setup;                     // virtual units charged per sequence start (stream-K weight)
+  // P32 sub-page tables (drafter attention): when set, group g of logical page
+  // j of request b is sub-page sub_k[b][4 j + g] (V: sub_v) of the pool, and
+  // page_table is not read.  num_subpages bounds the entries.
+  const int32_t* sub_k;
+  const int32_t* sub_v;
+  int num_subpages;
 };
 
 struct ProxyParams {
@@ -94,6 +100,21 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Entry i of a P32 sub-page table (sub-page i % (4 max_pages) of its
+// request, positions from 32 that on), used when that sub-page starts below
+// the request's length L; an unused entry is not read and gives sub-page 0,
+// a used entry outside [0, limit) flags the error word and gives sub-page 0.
+__device__ __forceinline__ int p32_entry(const int32_t* tab, int64_t i, int j, int L, int limit,
+                                         int* err) {
+  if (j * 32 >= L) return 0;
+  int s = tab[i];
+  if (s < 0 || s >= limit) {
+    atomicOr(err, TRTV_DEVERR_PAGE_ID);
+    s = 0;
+  }
+  return s;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

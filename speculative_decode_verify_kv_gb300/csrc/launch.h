@@ -50,6 +50,13 @@ cudaError_t launch_stage_kv(const void* k_new, const void* v_new, void* pool, co
                             int num_slots, int stride, bool fp8, float k_scale, float v_scale, int* err,
                             cudaStream_t st);
 
+// Flat (CSR) page table <-> padded table, row bases from the lengths:
+// to_flat: src = padded table, dst = flat (indptr may be null);
+// else:    src = flat, dst = padded table (indptr unused).
+cudaError_t launch_flat_table(bool to_flat, const int32_t* src, const int32_t* lens, int batch,
+                              int qo_len, int max_pages, int32_t* dst, int32_t* indptr, int* err,
+                              cudaStream_t st);
+
 // Split-KV combine of the cut sequences, launched right after an attention
 // kernel with programmatic dependent launch (no-op for a single CTA).
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st);

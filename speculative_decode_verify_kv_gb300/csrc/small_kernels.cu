@@ -9,6 +9,8 @@
 //                         attention kernel's stream-K split cut
 //   stage_kv_kernel       writes the qo_len verify tokens' K and V into their
 //                         cache slots along the ladder
+//   flat_table_kernel     flat (CSR) page table <-> padded table, row bases
+//                         from the lengths
 #include "common.cuh"
 #include "launch.h"
 
@@ -434,6 +436,81 @@ __global__ void stage_kv_kernel(const __nv_bfloat16* __restrict__ k_new, const _
   }
 }
 
+// ---------------------------------------------------------------------------
+// Flat (CSR) page table ("Eagle3 for M3 MSA path + CUDA graphs
+// compatibility", verify commit, overlap-correction fix: the flat table's row
+// layout follows the lengths, so it is rebuilt from the corrected lengths).
+// Row b holds n_b = ceil(L_b / 128) pages (0 for L_b <= 0, max_pages past the
+// capacity) starting at base_b = sum_{b' < b} n_b'.
+//   TO_FLAT:  flat[base_b + j] = pt[b][j] for j < n_b, indptr[b + 1] = base_b + n_b
+//   else:     pt[b][j] = flat[base_b + j] for j < n_b, else 0 (slot 0)
+// CTA c owns rows [256 c, 256 c + 256): it sums the page counts of all earlier
+// rows, scans its own, then copies its rows' entries with coalesced loops.
+constexpr int kFlatRows = 256;
+
+__device__ __forceinline__ int flat_pages(int L, int max_pages) {
+  if (L <= 0) return 0;
+  const int64_t n = (static_cast<int64_t>(L) + kPage - 1) / kPage;
+  return n > max_pages ? max_pages : static_cast<int>(n);
+}
+
+template <bool TO_FLAT>
+__global__ void __launch_bounds__(kFlatRows)
+    flat_table_kernel(const int32_t* __restrict__ src, const int32_t* __restrict__ lens, int batch,
+                      int qo_len, int max_pages, int32_t* __restrict__ dst, int32_t* __restrict__ indptr,
+                      int* err) {
+  __shared__ int warp_tot[kFlatRows / 32];
+  __shared__ int row_base[kFlatRows], row_n[kFlatRows];
+  pdl_wait();
+  pdl_trigger();
+  const int r0 = blockIdx.x * kFlatRows;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int before = 0;
+  for (int b = threadIdx.x; b < r0; b += kFlatRows) before += flat_pages(lens[b], max_pages);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  if (lane == 0) warp_tot[warp] = before;
+  __syncthreads();
+  int base = 0;
+#pragma unroll
+  for (int w = 0; w < kFlatRows / 32; ++w) base += warp_tot[w];
+  __syncthreads();
+  const int b = r0 + threadIdx.x;
+  int n = 0;
+  if (b < batch) {
+    const int L = lens[b];
+    n = flat_pages(L, max_pages);
+    if (!len_valid(L, qo_len, max_pages)) atomicOr(err, TRTV_DEVERR_KV_LEN);
+  }
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  row_base[threadIdx.x] = base + incl - n;
+  row_n[threadIdx.x] = n;
+  if (TO_FLAT && indptr != nullptr && b < batch) {
+    indptr[b + 1] = base + incl;
+    if (b == 0) indptr[0] = 0;
+  }
+  __syncthreads();
+  const int rows = min(kFlatRows, batch - r0);
+  const int total = rows * max_pages;
+  for (int e = threadIdx.x; e < total; e += kFlatRows) {
+    const int r = e / max_pages, j = e % max_pages;
+    const int64_t ti = static_cast<int64_t>(r0 + r) * max_pages + j;
+    if (TO_FLAT) {
+      if (j < row_n[r]) dst[row_base[r] + j] = src[ti];
+    } else {
+      dst[ti] = j < row_n[r] ? src[row_base[r] + j] : 0;
+    }
+  }
+}
+
 cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t* k_sub,
                                 int32_t* v_sub, int batch, int qo_len, int max_pages,
                                 int num_slots, int stride, int* err, cudaStream_t st) {
@@ -492,6 +569,16 @@ cudaError_t launch_stage_kv(const void* k_new, const void* v_new, void* pool, co
                           batch, qo_len, Hk, D, max_pages, num_slots, stride, k_scale, v_scale, err)
              : launch_pdl(stage_kv_kernel<false>, dim3(blocks), dim3(threads), 0, st, kn, vn, pool, pt, lens,
                           batch, qo_len, Hk, D, max_pages, num_slots, stride, k_scale, v_scale, err);
+}
+
+cudaError_t launch_flat_table(bool to_flat, const int32_t* src, const int32_t* lens, int batch,
+                              int qo_len, int max_pages, int32_t* dst, int32_t* indptr, int* err,
+                              cudaStream_t st) {
+  const dim3 grid((batch + kFlatRows - 1) / kFlatRows);
+  return to_flat ? launch_pdl(flat_table_kernel<true>, grid, dim3(kFlatRows), 0, st, src, lens, batch,
+                              qo_len, max_pages, dst, indptr, err)
+                 : launch_pdl(flat_table_kernel<false>, grid, dim3(kFlatRows), 0, st, src, lens, batch,
+                              qo_len, max_pages, dst, indptr, err);
 }
 
 }  // namespace trtv

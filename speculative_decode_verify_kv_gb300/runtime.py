@@ -14,8 +14,10 @@ from typing import Optional
 
 import torch
 
-from . import (TRTV_BF16, TRTV_F32, geom_of, trtv_msa_proxy_score, trtv_msa_sparse_attn, trtv_stage_kv,
-               trtv_msa_topk, trtv_subpage_view, trtv_verify_dense, trtv_workspace_bytes)
+from . import (TRTV_BF16, TRTV_F32, geom_of, trtv_draft_attn_p32, trtv_flatten_page_table,
+               trtv_msa_proxy_score, trtv_msa_sparse_attn, trtv_msa_topk, trtv_page_table_from_flat,
+               trtv_stage_kv, trtv_subpage_view, trtv_verify_dense, trtv_verify_dense_flat,
+               trtv_workspace_bytes, trtv_workspace_bytes_flat)
 from .workloads import VerifyProblem
 
 
@@ -41,7 +43,9 @@ class DeviceVerify:
                                p.max_pages_per_req)
         self.out = torch.empty(B * T, Hq, D, device=dev,
                                dtype=torch.float32 if self.out_dtype == TRTV_F32 else torch.bfloat16)
-        self.ws_bytes = trtv_workspace_bytes(self.geom, max(self.topk, 0))
+        # room for the sparse plan and for a rebuilt flat table
+        self.ws_bytes = max(trtv_workspace_bytes(self.geom, max(self.topk, 0)),
+                            trtv_workspace_bytes_flat(self.geom))
         if self.ws_bytes == 0:
             raise RuntimeError("geometry rejected by trtv_workspace_bytes")
         # no initial contents needed: each call writes what it reads
@@ -51,6 +55,8 @@ class DeviceVerify:
         self.block_idx = torch.empty(B, T, Hk, k, dtype=torch.int32, device=dev)
         self.k_sub = torch.empty(B, 4 * NP, dtype=torch.int32, device=dev)
         self.v_sub = torch.empty(B, 4 * NP, dtype=torch.int32, device=dev)
+        self.flat = torch.zeros(B * NP, dtype=torch.int32, device=dev)
+        self.indptr = torch.zeros(B + 1, dtype=torch.int32, device=dev)
 
     # -- single steps -------------------------------------------------------
     def subpage_view(self, stream=None):
@@ -84,6 +90,32 @@ class DeviceVerify:
         tensors) into their cache slots of this problem's pool."""
         trtv_stage_kv(self.geom, k_new, v_new, self.pool, self.page_table, self.kv_lens, stream)
         return self.pool
+
+    def flatten(self, stream=None):
+        """Restage the flat (CSR) table and indptr from the page table and the
+        current lengths."""
+        trtv_flatten_page_table(self.geom, self.page_table, self.kv_lens, self.flat, self.indptr, stream)
+        return self.flat, self.indptr
+
+    def table_from_flat(self, flat=None, out=None, stream=None):
+        out = torch.empty_like(self.page_table) if out is None else out
+        trtv_page_table_from_flat(self.geom, self.flat if flat is None else flat, self.kv_lens, out, stream)
+        return out
+
+    def dense_flat(self, flat=None, stream=None):
+        """Dense verify taking the flat table (rebuilt on the device)."""
+        trtv_verify_dense_flat(self.geom, self.q, self.pool, self.flat if flat is None else flat,
+                               self.kv_lens, self.out, self.out_dtype, self.workspace, self.ws_bytes,
+                               stream)
+        return self.out
+
+    def draft(self, k_sub=None, v_sub=None, stream=None):
+        """Attention through the P32 sub-page tables (default: this object's
+        k_sub / v_sub, as filled by subpage_view)."""
+        trtv_draft_attn_p32(self.geom, self.q, self.pool, self.k_sub if k_sub is None else k_sub,
+                            self.v_sub if v_sub is None else v_sub, self.kv_lens, self.out,
+                            self.out_dtype, self.workspace, self.ws_bytes, stream)
+        return self.out
 
     def msa(self, stream=None):
         """The MSA sparse verify pass: proxy scores -> per-token top-k -> sparse attention."""

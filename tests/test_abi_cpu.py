@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(trtv_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(trtv_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -98,3 +98,24 @@ def test_stage_kv_argument_checks(lib):
     assert lib.trtv_stage_kv(ctypes.byref(g), 16, 16, 24, 16, 16, None) == 1
     bad = geom(slot_stride=1)
     assert lib.trtv_stage_kv(ctypes.byref(bad), 16, 16, 16, 16, 16, None) == 1
+
+
+def test_flat_table_and_draft_argument_checks(lib):
+    g = geom()
+    need = lib.trtv_workspace_bytes(ctypes.byref(g), 0)
+    # the rebuilt padded table (2 x 3 int32) takes one more 256-byte region
+    need_flat = lib.trtv_workspace_bytes_flat(ctypes.byref(g))
+    assert need_flat == need + 256
+    assert lib.trtv_verify_dense_flat(ctypes.byref(g), 16, 16, 16, 16, 16, 0, 256, need, None) == 4
+    assert lib.trtv_verify_dense_flat(ctypes.byref(g), 16, 16, 0, 16, 16, 0, 256, need_flat, None) == 1
+    assert lib.trtv_verify_dense_flat(ctypes.byref(g), 16, 16, 16, 0, 16, 0, 256, need_flat, None) == 1
+    assert lib.trtv_draft_attn_p32(ctypes.byref(g), 16, 16, 0, 16, 16, 16, 0, 256, need, None) == 1
+    assert lib.trtv_draft_attn_p32(ctypes.byref(g), 16, 16, 16, 0, 16, 16, 0, 256, need, None) == 1
+    assert lib.trtv_draft_attn_p32(ctypes.byref(g), 16, 16, 16, 16, 16, 16, 0, 256, need - 1, None) == 4
+    assert lib.trtv_draft_attn_p32(ctypes.byref(g), 16, 8, 16, 16, 16, 16, 0, 256, need, None) == 1
+    assert lib.trtv_flatten_page_table(ctypes.byref(g), 0, 16, 16, 16, None) == 1
+    assert lib.trtv_flatten_page_table(ctypes.byref(g), 16, 16, 0, None, None) == 1
+    assert lib.trtv_page_table_from_flat(ctypes.byref(g), 16, 16, 0, None) == 1
+    assert lib.trtv_page_table_from_flat(ctypes.byref(geom(batch=0)), 16, 16, 16, None) == 1
+    assert lib.trtv_flatten_page_table(ctypes.byref(geom(batch=70000)), 16, 16, 16, None, None) == 2
+    assert lib.trtv_workspace_bytes_flat(ctypes.byref(geom(batch=0))) == 0
