@@ -18,6 +18,11 @@ roofline   the dominant call (trtv_verify_dense: the attention kernel and its
 cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 stage_kv   trtv_stage_kv (the verify tokens' K/V written into their slots),
            timed on its own copy of the pool, outside the step
+flat_table the flat (CSR) page-table calls on the headline workload: restaging
+           the flat table, and the dense verify taking it
+paths      extra workloads: msa, fp8, long, and draft (the drafter's qo_len-1
+           decode over an FP8 layer with slot stride 8, read through the P32
+           sub-page tables by trtv_draft_attn_p32)
 
 --impl reference runs the fp64 oracle as the reference arm (there is no
 runnable reference implementation; see the design notes).
@@ -192,14 +197,16 @@ def make(name):
 
 
 def describe(p, name):
+    view = ("read through the P32 sub-page tables (drafter attention)" if name == "draft"
+            else "P128 pages via P32 grouped-HND view")
     return {"workload": f"{name}: batch {p.batch}, qo_len {p.qo_len}, {p.num_q_heads}/{p.num_kv_heads} "
-                        f"heads, head_dim {p.head_dim}, {p.kv_dtype} K/V, P128 pages via P32 "
-                        f"grouped-HND view, stride {p.slot_stride}" + (f", top-k {p.topk}" if p.topk else ""),
+                        f"heads, head_dim {p.head_dim}, {p.kv_dtype} K/V, {view}, stride "
+                        f"{p.slot_stride}" + (f", top-k {p.topk}" if p.topk else ""),
             "batch": p.batch, "qo_len": p.qo_len, "num_q_heads": p.num_q_heads,
             "num_kv_heads": p.num_kv_heads, "head_dim": p.head_dim, "kv_dtype": p.kv_dtype,
             "kv_len_mean": float(p.kv_lens.float().mean()), "kv_len_total": int(p.kv_lens.sum()),
             "pool_slots": p.num_slots, "max_pages_per_req": p.max_pages_per_req,
-            "seed": 1000 + ["tiny", "dense", "msa", "fp8", "long"].index(name)}
+            "seed": 1000 + ["tiny", "dense", "msa", "fp8", "long", "draft"].index(name)}
 
 
 def time_path(name, steps, warmup, sampler=None):
@@ -213,9 +220,13 @@ def time_path(name, steps, warmup, sampler=None):
     p = make(name)
     dv = DeviceVerify(p)
     msa = p.topk > 0
+    draft = name == "draft"
     if msa:
         calls = [("proxy", dv.proxy), ("topk", dv.select), ("sparse", dv.sparse)]
         launches = 5   # proxy, top-k, sparse plan, attention, split combine
+    elif draft:
+        calls = [("subpage_view", dv.subpage_view), ("draft_attn", dv.draft)]
+        launches = 3   # sub-page view, attention through the P32 tables, split combine
     else:
         calls = [("subpage_view", dv.subpage_view), ("verify_dense", dv.dense)]
         launches = 3   # sub-page view, attention, split combine
@@ -258,9 +269,38 @@ def time_path(name, steps, warmup, sampler=None):
         res["bytes"] = {"proxy": proxy_bytes(p), "sparse": sb, "topk": p.batch * p.qo_len * p.num_kv_heads * (p.max_pages_per_req * 4 + p.topk * 4)}
         res["unique_blocks_mean"] = umean
     else:
-        res["bytes"] = {"verify_dense": dense_bytes(p),
+        res["bytes"] = {"draft_attn" if draft else "verify_dense": dense_bytes(p),
                         "subpage_view": p.batch * p.max_pages_per_req * (4 + 32) + p.batch * 4}
     return res
+
+
+def time_flat(name, steps, warmup):
+    """The flat (CSR) page-table entry points on workload `name`: restaging
+    the flat table from the lengths, and the dense verify taking the flat
+    table (its rebuild kernel + attention + combine) next to the verify on the
+    padded table."""
+    import torch
+    from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
+    p = make(name)
+    dv = DeviceVerify(p)
+    dv.flatten()
+    calls = [("flatten", dv.flatten), ("verify_dense_flat", dv.dense_flat), ("verify_dense", dv.dense)]
+    out = {}
+    for n, f in calls:
+        for _ in range(warmup):
+            f()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            f()
+        e.record()
+        torch.cuda.synchronize()
+        out[n + "_ms"] = s.elapsed_time(e) / steps
+    out["launches"] = {"flatten": 1, "verify_dense_flat": 3, "verify_dense": 2}
+    del dv
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_stage(name, steps, warmup):
@@ -415,8 +455,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="dense", choices=["dense", "msa", "fp8", "long"])
-    ap.add_argument("--paths", default="msa,fp8,long",
+    ap.add_argument("--workload", default="dense", choices=["dense", "msa", "fp8", "long", "draft"])
+    ap.add_argument("--paths", default="msa,fp8,long,draft",
                     help="extra workloads timed alongside (comma list, or none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -462,7 +502,7 @@ def main():
     value = qtok * world / (ms / 1e3)
 
     peak, peak_kind = peaks()
-    dom = "proxy" if p.topk else "verify_dense"
+    dom = "proxy" if p.topk else ("draft_attn" if args.workload == "draft" else "verify_dense")
     dom_ms = head["per_call_ms"][dom]
     dom_bytes = head["bytes"][dom]
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -499,6 +539,7 @@ def main():
         torch.cuda.empty_cache()
 
     stage = time_stage(args.workload, max(10, args.steps // 8), args.warmup)
+    flat = None if p.topk else time_flat(args.workload, max(10, args.steps // 8), args.warmup)
 
     e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)
     if dist and e2e:
@@ -520,7 +561,8 @@ def main():
             "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
                     if e2e else None),
             "gpu_launches": head["launches_per_step"] * args.steps, "clocks": clocks,
-            "device_error": head["device_error"], "paths": paths, "stage_kv": stage}
+            "device_error": head["device_error"], "paths": paths, "stage_kv": stage,
+            "flat_table": flat}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:

@@ -99,7 +99,8 @@ def make_problem(*, name: str = "custom", kv_lens: Sequence[int], qo_len: int,
                  slot_stride: int = 2, kv_dtype: str = BF16, sm_scale: Optional[float] = None,
                  topk: int = 0, out_dtype: str = "bf16", seed: int = 0,
                  slack_slots: int = 0, fill_unused_with=None,
-                 shift_fraction: float = 0.0, shift_value: float = 0.0) -> VerifyProblem:
+                 shift_fraction: float = 0.0, shift_value: float = 0.0,
+                 other_buffers=None) -> VerifyProblem:
     """Build one seeded problem.
 
     Page ids are a random permutation of the pool's slots handed to requests in
@@ -107,6 +108,9 @@ def make_problem(*, name: str = "custom", kv_lens: Sequence[int], qo_len: int,
     ``float('nan')``) fills every buffer of slots no request uses.
     ``shift_fraction`` of each request's pages get ``shift_value`` added to all
     K elements of that slot (the long-context workload's distinct winners).
+    ``other_buffers`` (a float): buffers 2.. of every used slot -- the pages of
+    other layers in a pool with a wider slot stride -- hold that value instead
+    of random draws (only this layer's K and V pages are drawn).
     """
     B = len(kv_lens)
     lens = torch.tensor(list(kv_lens), dtype=torch.int32)
@@ -129,11 +133,12 @@ def make_problem(*, name: str = "custom", kv_lens: Sequence[int], qo_len: int,
     Hq, Hk, D, T = num_q_heads, num_kv_heads, head_dim, qo_len
     q = _randn_bf16(B * T * Hq * D, gen).view(B * T, Hq, D)
     buf_elems = GROUPS * Hk * SUBPAGE * D
-    slot_elems = slot_stride * buf_elems
     used = torch.unique(torch.cat([perm[:total].to(torch.int64), torch.zeros(1, dtype=torch.int64)]))
     n_used = used.numel()
-    vals = _randn_f32(n_used * slot_elems, gen) if kv_dtype == FP8 else _randn_bf16(n_used * slot_elems, gen)
-    vals = vals.view(n_used, slot_stride, buf_elems)
+    n_draw = slot_stride if other_buffers is None else min(2, slot_stride)
+    n_vals = n_used * n_draw * buf_elems
+    vals = _randn_f32(n_vals, gen) if kv_dtype == FP8 else _randn_bf16(n_vals, gen)
+    vals = vals.view(n_used, n_draw, buf_elems)
     shifted = None
     if shift_fraction > 0.0:
         pick = []
@@ -155,13 +160,15 @@ def make_problem(*, name: str = "custom", kv_lens: Sequence[int], qo_len: int,
     else:
         pool_dtype = torch.bfloat16
     pool = torch.zeros(num_slots, slot_stride, buf_elems, dtype=pool_dtype)
-    if fill_unused_with is not None:
+    def stored(x):
         if kv_dtype == FP8:
-            code = torch.tensor([fill_unused_with], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
-            pool.fill_(int(code.item()))
-        else:
-            pool.fill_(fill_unused_with)
-    pool[used] = vals
+            return int(torch.tensor([x], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).item())
+        return x
+    if fill_unused_with is not None:
+        pool.fill_(stored(fill_unused_with))
+    if n_draw < slot_stride:
+        pool[used, n_draw:] = stored(other_buffers)
+    pool[used, :n_draw] = vals
     pool = pool.view(num_slots * slot_stride, GROUPS, Hk, SUBPAGE, D)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
@@ -184,12 +191,13 @@ def _lognormal_lens(gen: torch.Generator, B: int, median: float, sigma: float,
     return L.tolist()
 
 
-WORKLOADS = ("tiny", "dense", "msa", "fp8", "long")
+WORKLOADS = ("tiny", "dense", "msa", "fp8", "long", "draft")
 
 
 def make_workload(name: str, *, batch: Optional[int] = None, seed: Optional[int] = None,
                   **overrides) -> VerifyProblem:
-    """The five verify workloads by name; ``batch`` keeps the first requests only
+    """The verify workloads by name (the five configurations plus the drafter's
+    P32 decode step, "draft"); ``batch`` keeps the first requests only
     (same lens, same draws for them) so a test can run a reduced copy."""
     idx = WORKLOADS.index(name)
     s = 1000 + idx if seed is None else seed
@@ -211,6 +219,12 @@ def make_workload(name: str, *, batch: Optional[int] = None, seed: Optional[int]
         kw = dict(kv_lens=[131072] * 8, qo_len=8, num_q_heads=64, num_kv_heads=4, head_dim=128,
                   max_pages_per_req=1024, slack_slots=1024, topk=32, shift_fraction=0.05,
                   shift_value=2.0)
+    elif name == "draft":
+        # the drafter's decode step over its FP8 layer, read through the P32
+        # tables; slots hold eight page buffers (layer-local stride 8)
+        kw = dict(kv_lens=_uniform_lens(lgen, 64, 1024, 8192), qo_len=1, num_q_heads=32,
+                  num_kv_heads=4, head_dim=128, max_pages_per_req=64, slack_slots=1024,
+                  slot_stride=8, kv_dtype=FP8, other_buffers=0.0)
     else:
         raise KeyError(name)
     if batch is not None:
