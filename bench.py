@@ -20,7 +20,8 @@ stage_kv   trtv_stage_kv (the verify tokens' K/V written into their slots),
            timed on its own copy of the pool, outside the step
 flat_table the flat (CSR) page-table calls on the headline workload: restaging
            the flat table, and the dense verify taking it
-paths      extra workloads: msa, fp8, long, and draft (the drafter's qo_len-1
+paths      extra workloads (msa and long also timed with trtv_msa_select, the
+           top-k fused into the proxy kernel): msa, fp8, long, and draft (the drafter's qo_len-1
            decode over an FP8 layer with slot stride 8, read through the P32
            sub-page tables by trtv_draft_attn_p32)
 
@@ -303,6 +304,36 @@ def time_flat(name, steps, warmup):
     return out
 
 
+def time_msa_fused(name, steps, warmup):
+    """The MSA pass with proxy and top-k in one call (trtv_msa_select, the
+    top-k fused into the proxy kernel) followed by the sparse attention: the
+    step time, and the select call on its own."""
+    import torch
+    from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
+    p = make(name)
+    dv = DeviceVerify(p)
+    out = {}
+    for label, calls in (("step", [dv.select_fused, dv.sparse]), ("select", [dv.select_fused])):
+        for _ in range(warmup):
+            for f in calls:
+                f()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            for f in calls:
+                f()
+        e.record()
+        torch.cuda.synchronize()
+        out[label + "_ms"] = s.elapsed_time(e) / steps
+    out["launches_per_step"] = 4   # proxy with fused top-k, sparse plan, attention, combine
+    from speculative_decode_verify_kv_gb300 import trtv_get_device_error
+    out["device_error"] = trtv_get_device_error()
+    del dv
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_stage(name, steps, warmup):
     """trtv_stage_kv on workload `name`: the qo_len new tokens' K and V of
     every request written into their cache slots (device-resident inputs)."""
@@ -533,6 +564,8 @@ def main():
             pv["unique_blocks_mean"] = r["unique_blocks_mean"]
         if not pe.topk:
             pv["stage_kv"] = time_stage(extra, max(10, args.steps // 8), args.warmup)
+        else:
+            pv["fused_select"] = time_msa_fused(extra, max(10, args.steps // 8), args.warmup)
         paths[extra] = pv
         del r
         _CACHE.pop(extra, None)

@@ -194,6 +194,27 @@ trtv_status trtv_msa_topk(const trtv_geom* geom, const float* scores, const int3
                           int32_t topk, int32_t* block_idx, void* stream);
 
 /*
+ * Proxy scores and per-token top-k in one call (the same results as
+ * trtv_msa_proxy_score followed by trtv_msa_topk; source: PR #3 "... verify"
+ * commit, capture-safe device-only pipeline).  When the tcgen05 proxy kernel
+ * applies (bf16 K, head_dim 128, power-of-two G <= 16, G * qo_len <= 128) the
+ * top-k runs inside it: the CTA that completes the last page of a (request,
+ * KV head) sequence selects that sequence's qo_len rows, so no top-k kernel
+ * is launched; otherwise the top-k kernel follows the proxy kernel.
+ *   scores     fp32 [B, T, Hk, max_pages] (written, as trtv_msa_proxy_score)
+ *   block_idx  int32 [B, T, Hk, topk] (written, as trtv_msa_topk)
+ *   workspace  >= trtv_workspace_bytes(geom, topk) bytes, 256-byte aligned; a
+ *              per-sequence page counter in it is zeroed by an asynchronous
+ *              memset on `stream` before the kernel (no initial contents
+ *              needed).  1 <= topk <= 1024.
+ * Errors as trtv_msa_proxy_score and trtv_msa_topk, plus TRTV_ERR_WORKSPACE.
+ */
+trtv_status trtv_msa_select(const trtv_geom* geom, const void* q, const void* kv_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, int32_t topk,
+                            float* scores, int32_t* block_idx, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/*
  * Sparse GQA attention over the selected blocks (source: PR #3 "... verify"
  * commit).  As trtv_verify_dense, with token t of request b attending only
  * positions inside the blocks block_idx[b][t][h][0..topk) (entries < 0 are

@@ -110,7 +110,7 @@ struct Plan {
   int group, group_pad, rows, mt, rows_pad, num_ctas, n_seq;
   int64_t pool_rows;
   // workspace
-  size_t ws_o, ws_lse, ws_splits, ws_blocks, ws_masks, ws_count, ws_total;
+  size_t ws_o, ws_lse, ws_splits, ws_blocks, ws_masks, ws_count, ws_sel, ws_total;
   int plan_cap;
 };
 
@@ -156,6 +156,8 @@ trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
   p.ws_masks = off;
   off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(uint32_t), 256);
   p.ws_count = off;
+  off = align_up(off + (topk > 0 ? static_cast<size_t>(p.n_seq) * sizeof(int32_t) : 0), 256);
+  p.ws_sel = off;  // fused proxy + top-k: pages done per sequence
   off = align_up(off + (topk > 0 ? static_cast<size_t>(p.n_seq) * sizeof(int32_t) : 0), 256);
   p.ws_total = off;
   *pl = p;
@@ -299,20 +301,25 @@ bool proxy_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
          pl.group <= 16 && pl.group * g->qo_len <= 128 && aligned(q, 16);
 }
 
-bool plan_proxy_umma_smem(const trtv_geom* g, ProxyParams* a, size_t* bytes) {
-  const size_t qbufs = 2 * 128 * 128 * 2;
+// fused: room for the fused top-k's histograms (8 warps x 1 KB).
+bool plan_proxy_umma_smem(const trtv_geom* g, const Plan& pl, bool fused, ProxyParams* a, size_t* bytes) {
+  const size_t qbuf = pl.group * g->qo_len <= 64 ? 64 * 128 * 2 : 128 * 128 * 2;
+  const size_t qbufs = 2 * qbuf;
+  const size_t hist = fused ? 8 * 256 * sizeof(uint32_t) : 0;
   const size_t stage = static_cast<size_t>(kGroups) * 2 * kBox;
   const size_t scan = align_up((static_cast<size_t>(g->batch) + 1 + 32) * sizeof(int32_t), 16);
   const size_t budget = kSmemOptin - kAlignSlack - 1024;
-  const size_t fixed = qbufs + scan + (2 * 8 + 9) * sizeof(uint64_t) + 16;
+  const size_t fixed = qbufs + hist + scan + (2 * 8 + 9) * sizeof(uint64_t) + 16;
   if (fixed + 2 * stage > budget) return false;
   int nst = static_cast<int>((budget - fixed) / stage);
   if (nst > 6) nst = 6;
   a->off_q = 0;
+  a->qbuf = static_cast<int>(qbuf);
   a->off_stage = static_cast<int>(qbufs);
   a->stage_bytes = static_cast<int>(stage);
   size_t off = qbufs + static_cast<size_t>(nst) * stage;
-  a->off_red = 0;
+  a->off_red = static_cast<int>(off);
+  off += hist;
   a->off_scan = static_cast<int>(off);
   off += scan;
   a->off_bar = static_cast<int>(align_up(off, 8));
@@ -556,23 +563,33 @@ trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const voi
                      block_idx, topk, out, out_dtype, workspace, ws_bytes, stream);
 }
 
-trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* kv_pool,
-                                 const int32_t* page_table, const int32_t* kv_lens, float* scores,
-                                 void* stream) {
+namespace {
+// Proxy scores, and with block_idx set the per-token top-k as well: fused
+// into the tcgen05 proxy kernel when that kernel applies (the sequence
+// counters in the workspace zeroed first), else the top-k kernel after it.
+trtv_status proxy_common(const trtv_geom* g, const void* q, const void* kv_pool, const int32_t* page_table,
+                         const int32_t* kv_lens, float* scores, int32_t topk, int32_t* block_idx, void* ws,
+                         size_t ws_bytes, void* stream) {
+  const bool select = block_idx != nullptr;
   Plan pl;
-  trtv_status s = make_plan(g, 0, &pl);
+  trtv_status s = make_plan(g, select ? topk : 0, &pl);
   if (s != TRTV_OK) return s;
   if (pl.group > 16) return TRTV_ERR_UNSUPPORTED;
   if (q == nullptr || kv_pool == nullptr || page_table == nullptr || kv_lens == nullptr ||
       scores == nullptr)
     return TRTV_ERR_INVALID_ARG;
   if (!aligned(kv_pool, 16) || !aligned(q, 8) || !aligned(scores, 4)) return TRTV_ERR_INVALID_ARG;
+  if (select) {
+    if (topk < 1 || topk > 1024) return TRTV_ERR_INVALID_ARG;
+    if (g->max_pages_per_req > 16384) return TRTV_ERR_UNSUPPORTED;
+    if (ws == nullptr || !aligned(ws, 256) || ws_bytes < pl.ws_total) return TRTV_ERR_WORKSPACE;
+  }
   int* err = err_word();
   if (err == nullptr) return TRTV_ERR_CUDA;
   ProxyParams a{};
   size_t smem = 0;
   const bool umma = proxy_umma_eligible(g, pl, q);
-  if (umma ? !plan_proxy_umma_smem(g, &a, &smem) : !plan_proxy_smem(g, pl, &a, &smem))
+  if (umma ? !plan_proxy_umma_smem(g, pl, select, &a, &smem) : !plan_proxy_smem(g, pl, &a, &smem))
     return TRTV_ERR_UNSUPPORTED;
   CUtensorMap map, qmap;
   if (!encode_pool_map(g, pl, kv_pool, &map)) return TRTV_ERR_CUDA;
@@ -597,12 +614,38 @@ trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* 
   a.num_ctas = pl.num_ctas;
   a.score_scale = g->sm_scale * g->k_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e =
-      umma ? launch_proxy_umma(map, qmap, a, pl.num_ctas, smem, st)
-           : g->kv_dtype == TRTV_FP8_E4M3
-                 ? launch_proxy_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
-                 : launch_proxy_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  const bool fused = select && umma;
+  if (fused) {
+    a.topk_out = block_idx;
+    a.topk = topk;
+    a.seq_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + pl.ws_sel);
+    if (cudaMemsetAsync(a.seq_count, 0, static_cast<size_t>(pl.n_seq) * sizeof(int32_t), st) != cudaSuccess)
+      return TRTV_ERR_CUDA;
+  }
+  cudaError_t e = umma ? launch_proxy_umma(map, qmap, a, pl.num_ctas, smem, st)
+                       : g->kv_dtype == TRTV_FP8_E4M3
+                             ? launch_proxy_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)
+                             : launch_proxy_bf16(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st);
+  if (e != cudaSuccess) return TRTV_ERR_CUDA;
+  if (select && !fused)
+    e = launch_topk(scores, kv_lens, g->batch, g->qo_len, g->num_kv_heads, g->max_pages_per_req, topk,
+                    block_idx, err, st);
   return e == cudaSuccess ? TRTV_OK : TRTV_ERR_CUDA;
+}
+}  // namespace
+
+trtv_status trtv_msa_proxy_score(const trtv_geom* g, const void* q, const void* kv_pool,
+                                 const int32_t* page_table, const int32_t* kv_lens, float* scores,
+                                 void* stream) {
+  return proxy_common(g, q, kv_pool, page_table, kv_lens, scores, 0, nullptr, nullptr, 0, stream);
+}
+
+trtv_status trtv_msa_select(const trtv_geom* g, const void* q, const void* kv_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, int32_t topk, float* scores,
+                            int32_t* block_idx, void* workspace, size_t ws_bytes, void* stream) {
+  if (block_idx == nullptr) return TRTV_ERR_INVALID_ARG;
+  return proxy_common(g, q, kv_pool, page_table, kv_lens, scores, topk, block_idx, workspace, ws_bytes,
+                      stream);
 }
 
 trtv_status trtv_msa_topk(const trtv_geom* g, const float* scores, const int32_t* kv_lens,

@@ -87,7 +87,15 @@ struct ProxyParams {
   int max_pages, num_slots, slot_stride, rows, rows_pad, num_ctas, nstages;
   float score_scale;    // sm_scale * k_scale (> 0, so it commutes with max)
   int off_stage, stage_bytes, off_red, off_scan, off_bar;
-  int off_q;            // tcgen05 path: two Q tiles of 128 rows x 128 bf16
+  int off_q;            // tcgen05 path: two Q tiles of qbuf bytes (64 or 128 rows x 128 bf16)
+  int qbuf;
+  // fused top-k (tcgen05 path): when topk_out is set, the CTA that finishes
+  // the last page of a (request, KV head) sequence selects its rows' blocks
+  // (8 warps x 256 histogram words at off_red); seq_count[b * Hk + h] counts
+  // the pages done (zero before the launch)
+  int32_t* topk_out;
+  int32_t* seq_count;
+  int topk;
 };
 
 // ---- small helpers -------------------------------------------------------

@@ -24,9 +24,15 @@
 //   warps 0-7  two epilogue warpgroups take alternate pages: tcgen05.ld of
 //              their 128 rows x 128 columns, masked row maximum, maximum over
 //              each token's G rows (lane shuffles), one score per token.
+// Fused top-k (topk_out set): at the end of each sequence it touched, the CTA
+// adds its page count to the sequence's counter; the CTA that completes the
+// count selects the top-k blocks of the sequence's qo_len rows (topk_row, one
+// epilogue warp per row) from the scores every contributor wrote.  Requests
+// with no pages get rows of -1 from CTA b % grid.
 #pragma once
 
 #include "attn.cuh"
+#include "topk.cuh"
 #include "umma.cuh"
 
 namespace trtv {
@@ -41,7 +47,10 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
                       const __grid_constant__ ProxyParams p) {
   static_assert(D == 128, "tcgen05 proxy handles head_dim 128");
   constexpr int STAGE = kGroups * 2 * kBox;  // one page of K for one head: 32 KB
-  constexpr int QBUF = 128 * D * 2;          // 128 rows x 128 bf16: 32 KB
+  // one Q tile: rows x 128 bf16 in two 64-column halves, 16 KB for at most
+  // 64 rows (the M = 128 UMMA then reads rows 64..127 from whatever follows
+  // the tile, into accumulator rows nobody reads), else 32 KB
+  const int QBUF = p.qbuf;
   constexpr uint32_t IDESC = umma_idesc_bf16(128, 128);
 
   extern __shared__ uint8_t smem_raw[];
@@ -60,6 +69,7 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
   int32_t* warp_tot = scan + p.batch + 1;
   const int Hk = p.num_kv_heads, T = p.qo_len, NP = p.max_pages, G = p.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int seq_last;
 
   pdl_wait();  // inputs may come from the previous kernel of the stream
   // -inf for every score no page pass writes (pages past the request's last
@@ -97,6 +107,13 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
   });
   const int64_t W = static_cast<int64_t>(scan[p.batch]) * Hk;
   pdl_trigger();
+  if (p.topk_out != nullptr) {  // rows of requests without pages select nothing
+    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+      if (scan[b + 1] != scan[b]) continue;
+      int32_t* o = p.topk_out + static_cast<int64_t>(b) * T * Hk * p.topk;
+      for (int e = threadIdx.x; e < T * Hk * p.topk; e += blockDim.x) o[e] = -1;
+    }
+  }
   if (W == 0) return;
   const int64_t u0 = cta_unit_begin(blockIdx.x, W, p.num_ctas);
   const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);
@@ -249,6 +266,27 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
         for (int off = 1; off < Gp; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (valid && gl == 0)
           p.scores[((static_cast<int64_t>(cur.b) * T + t) * Hk + cur.h) * NP + j] = m * p.score_scale;
+      }
+      if (p.topk_out != nullptr) {
+        // this CTA's scores of the sequence are written: publish, count, and
+        // let the CTA that completes the sequence select its rows
+        __threadfence();
+        named_barrier(1, 256);
+        if (threadIdx.x == 0) {
+          const int done = static_cast<int>(j1 - j0);
+          const int old = atomicAdd(&p.seq_count[cur.b * Hk + cur.h], done);
+          seq_last = old + done == cur.units;
+        }
+        named_barrier(1, 256);
+        if (seq_last) {
+          __threadfence();
+          for (int tt = warp; tt < T; tt += 8) {
+            const int64_t row = (static_cast<int64_t>(cur.b) * T + tt) * Hk + cur.h;
+            topk_row(p.scores + row * NP, (L - T + tt) / kPage + 1, p.topk, p.topk_out + row * p.topk,
+                     reinterpret_cast<uint32_t*>(smem + p.off_red) + warp * 256, lane);
+          }
+        }
+        named_barrier(1, 256);  // seq_last is rewritten for the next sequence
       }
     }
   }

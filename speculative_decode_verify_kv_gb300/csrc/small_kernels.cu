@@ -13,6 +13,7 @@
 //                         from the lengths
 #include "common.cuh"
 #include "launch.h"
+#include "topk.cuh"
 
 namespace trtv {
 
@@ -127,117 +128,26 @@ __global__ void sparse_plan_kernel(const int32_t* __restrict__ idx, const int32_
 }
 
 // ---------------------------------------------------------------------------
-// Per-token top-k ("Eagle3 for M3 MSA path + CUDA graphs compatibility",
-// verify commit: top-k gets per-token ladder valid-page counts).  One warp
-// per (b, t, h) row.  Keys: scores mapped to order-preserving uint32 (with
-// -0 folded into +0, so equal scores are equal keys).  A 4 x 8-bit radix
-// select finds the k-th largest key tau and how many of the k picks must be
-// equal to tau; a final ballot pass in ascending block order takes every key
-// > tau and the lowest-index keys == tau, which writes the output already in
-// ascending order.
-__device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-constexpr int kTopkCachedPages = 1024;  // 32 KB of keys per 8-warp block
-
+// Per-token top-k (the selection itself is topk_row, topk.cuh): one warp per
+// (b, t, h) row of n_t = floor((kv_len - qo_len + t) / 128) + 1 valid blocks;
+// rows of invalid requests are all -1.
 __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __restrict__ lens,
                             int batch, int qo_len, int num_kv_heads, int max_pages, int topk,
                             int32_t* __restrict__ out, int* err) {
   __shared__ uint32_t hist_all[8][256];
-  // rows of at most kTopkCachedPages scores keep their order keys in shared
-  // memory for the five passes; longer rows re-read them from global memory
-  extern __shared__ uint32_t keys_all[];  // [8 warps][max_pages] when cached
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   const int64_t nrows = static_cast<int64_t>(batch) * qo_len * num_kv_heads;
   if (row >= nrows) return;
-  uint32_t* hist = hist_all[warp];
   const int t = static_cast<int>((row / num_kv_heads) % qo_len);
   const int b = static_cast<int>(row / (static_cast<int64_t>(num_kv_heads) * qo_len));
   const int L = lens[b];
   int n = 0;
   if (len_valid(L, qo_len, max_pages)) n = (L - qo_len + t) / kPage + 1;
   else if (t == 0 && lane == 0 && (row % num_kv_heads) == 0) atomicOr(err, TRTV_DEVERR_KV_LEN);
-  const float* srow = scores + row * max_pages;
-  int32_t* orow = out + row * topk;
-  if (n <= topk) {
-    for (int i = lane; i < topk; i += 32) orow[i] = i < n ? i : -1;
-    return;
-  }
-  const bool cached = max_pages <= kTopkCachedPages;
-  uint32_t* keys = keys_all + warp * max_pages;
-  if (cached) {
-    for (int i = lane; i < n; i += 32) keys[i] = order_key(srow[i]);
-    __syncwarp();
-  }
-  auto key_at = [&](int i) -> uint32_t { return cached ? keys[i] : order_key(srow[i]); };
-  uint32_t prefix = 0, pmask = 0;
-  int remaining = topk;  // picks still to place among keys matching the prefix
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = lane; i < 256; i += 32) hist[i] = 0;
-    __syncwarp();
-    for (int i = lane; i < n; i += 32) {
-      const uint32_t key = key_at(i);
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-    }
-    __syncwarp();
-    // lane l owns digits 255 - 8l .. 248 - 8l (descending); counts from the top
-    uint32_t cnt[8];
-    uint32_t local = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      cnt[k] = hist[255 - 8 * lane - k];
-      local += cnt[k];
-    }
-    uint32_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const uint32_t above = incl - local;  // keys in higher digits than this lane's
-    int digit = -1;
-    uint32_t gt = 0;
-    if (above < static_cast<uint32_t>(remaining) && incl >= static_cast<uint32_t>(remaining)) {
-      uint32_t run = above;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (digit < 0 && run + cnt[k] >= static_cast<uint32_t>(remaining)) {
-          digit = 255 - 8 * lane - k;
-          gt = run;
-        }
-        run += cnt[k];
-      }
-    }
-    const unsigned owner = __ballot_sync(0xffffffffu, digit >= 0);
-    const int src = __ffs(owner) - 1;
-    digit = __shfl_sync(0xffffffffu, digit, src);
-    gt = __shfl_sync(0xffffffffu, gt, src);
-    prefix |= static_cast<uint32_t>(digit) << shift;
-    pmask |= 255u << shift;
-    remaining -= static_cast<int>(gt);
-    __syncwarp();
-  }
-  // tau = prefix; take all keys > tau and the first `remaining` keys == tau
-  int written = 0, eq_seen = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    uint32_t key = 0;
-    if (i < n) key = key_at(i);
-    const bool eq = i < n && key == prefix;
-    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-    const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
-    const bool sel = i < n && (key > prefix || (eq && eq_rank < remaining));
-    const unsigned selm = __ballot_sync(0xffffffffu, sel);
-    if (sel) orow[written + __popc(selm & ((1u << lane) - 1u))] = i;
-    written += __popc(selm);
-    eq_seen += __popc(eqm);
-  }
-  for (int i = written + lane; i < topk; i += 32) orow[i] = -1;
+  topk_row(scores + row * max_pages, n, topk, out + row * topk, hist_all[warp], lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -543,8 +453,7 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
                         cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(batch) * qo_len * num_kv_heads;
   const int blocks = static_cast<int>((rows + 7) / 8);
-  const size_t smem = max_pages <= kTopkCachedPages ? static_cast<size_t>(8) * max_pages * sizeof(uint32_t) : 0;
-  return launch_pdl(topk_kernel, dim3(blocks), dim3(256), smem, st, scores, lens, batch, qo_len, num_kv_heads,
+  return launch_pdl(topk_kernel, dim3(blocks), dim3(256), 0, st, scores, lens, batch, qo_len, num_kv_heads,
                     max_pages, topk, out, err);
 }
 

@@ -15,7 +15,8 @@ from typing import Optional
 import torch
 
 from . import (TRTV_BF16, TRTV_F32, geom_of, trtv_draft_attn_p32, trtv_flatten_page_table,
-               trtv_msa_proxy_score, trtv_msa_sparse_attn, trtv_msa_topk, trtv_page_table_from_flat,
+               trtv_msa_proxy_score, trtv_msa_select, trtv_msa_sparse_attn, trtv_msa_topk,
+               trtv_page_table_from_flat,
                trtv_stage_kv, trtv_subpage_view, trtv_verify_dense, trtv_verify_dense_flat,
                trtv_workspace_bytes, trtv_workspace_bytes_flat)
 from .workloads import VerifyProblem
@@ -78,6 +79,12 @@ class DeviceVerify:
                       self.topk, self.block_idx, stream)
         return self.block_idx
 
+    def select_fused(self, stream=None):
+        """Proxy scores and top-k in one call (trtv_msa_select)."""
+        trtv_msa_select(self.geom, self.q, self.pool, self.page_table, self.kv_lens, self.topk,
+                        self.scores, self.block_idx, self.workspace, self.ws_bytes, stream)
+        return self.block_idx
+
     def sparse(self, block_idx=None, topk: Optional[int] = None, stream=None):
         idx = self.block_idx if block_idx is None else block_idx
         k = self.topk if topk is None else topk
@@ -121,4 +128,9 @@ class DeviceVerify:
         """The MSA sparse verify pass: proxy scores -> per-token top-k -> sparse attention."""
         self.proxy(stream)
         self.select(stream=stream)
+        return self.sparse(stream=stream)
+
+    def msa_fused(self, stream=None):
+        """The same pass with proxy and top-k in one call."""
+        self.select_fused(stream)
         return self.sparse(stream=stream)

@@ -119,3 +119,17 @@ def test_flat_table_and_draft_argument_checks(lib):
     assert lib.trtv_page_table_from_flat(ctypes.byref(geom(batch=0)), 16, 16, 16, None) == 1
     assert lib.trtv_flatten_page_table(ctypes.byref(geom(batch=70000)), 16, 16, 16, None, None) == 2
     assert lib.trtv_workspace_bytes_flat(ctypes.byref(geom(batch=0))) == 0
+
+
+def test_msa_select_argument_checks(lib):
+    g = geom()
+    need = lib.trtv_workspace_bytes(ctypes.byref(g), 2)
+    # null outputs / bad k / small workspace are rejected on the host
+    assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 2, 16, 0, 256, need, None) == 1
+    assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 0, 16, 16, 256, need, None) == 1
+    assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 2000, 16, 16, 256, need, None) == 1
+    assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 2, 16, 16, 256, need - 1, None) == 4
+    assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 2, 16, 16, 128, need, None) == 4
+    assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 2, 0, 16, 256, need, None) == 1
+    big = geom(num_q_heads=64, num_kv_heads=2)  # group 32 > 16: no proxy
+    assert lib.trtv_msa_select(ctypes.byref(big), 16, 16, 16, 16, 2, 16, 16, 256, 1 << 30, None) == 2
