@@ -435,6 +435,24 @@ def cpu_baseline(name, budget_s=12.0):
                       f"({int(p.kv_lens[:len(reqs)].sum())} KV positions), one pass, {dt:.2f} s"}
 
 
+def max_over_ranks(x: float, dist=None, device="cuda") -> float:
+    """The largest of every rank's x: the job's step time is its slowest
+    replica's (each rank runs the whole workload on its own GPU; no data
+    crosses ranks)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job query tokens per second: every replica's tokens over the
+    slowest replica's step time."""
+    return tokens_per_rank * world / (ms / 1e3)
+
+
 def run_reference(args):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
     sample (4 requests, rotating) of the same workload."""
@@ -523,14 +541,10 @@ def main():
     head = time_path(args.workload, args.steps, args.warmup, sampler)
     sampler.stop()
     clocks = sampler.summary(head["t0"], head["t1"])
-    ms = head["ms_per_step"]
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(head["ms_per_step"], dist)
     p = head["p"]
     qtok = p.batch * p.qo_len
-    value = qtok * world / (ms / 1e3)
+    value = job_value(qtok, world, ms)
 
     peak, peak_kind = peaks()
     dom = "proxy" if p.topk else ("draft_attn" if args.workload == "draft" else "verify_dense")
@@ -576,9 +590,7 @@ def main():
 
     e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)
     if dist and e2e:
-        t = torch.tensor([e2e["ms_per_step"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["value"] = qtok * world / (float(t.item()) / 1e3)
+        e2e["value"] = job_value(qtok, world, max_over_ranks(e2e["ms_per_step"], dist))
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
