@@ -48,8 +48,9 @@
  *     kernels handle, TRTV_ERR_WORKSPACE when ws_bytes is too small, and
  *     TRTV_ERR_CUDA when a launch fails.  Nothing is enqueued on error.
  *   - Data errors are found on the device (kv_len < qo_len or beyond
- *     128 * max_pages_per_req; a used page id outside [0, num_slots); a
- *     top-k block index >= max_pages_per_req).  Affected output rows are
+ *     128 * max_pages_per_req; a used page id outside [0, num_slots) or a used
+ *     P32 sub-page index outside the view; a top-k block index >=
+ *     max_pages_per_req).  Affected output rows are
  *     zero (or, for a bad page id, finite but meaningless), no kernel traps,
  *     and a bit is set in a per-device error word read by
  *     trtv_get_device_error.
@@ -77,7 +78,8 @@ typedef enum { TRTV_BF16 = 0, TRTV_FP8_E4M3 = 1, TRTV_F32 = 2 } trtv_dtype;
 
 /* Device error word bits (trtv_get_device_error). */
 #define TRTV_DEVERR_KV_LEN 1    /* kv_len < qo_len or kv_len > 128 * max_pages */
-#define TRTV_DEVERR_PAGE_ID 2   /* a used page-table entry outside [0, num_slots) */
+#define TRTV_DEVERR_PAGE_ID 2   /* a used page-table entry outside [0, num_slots), or a used
+                                   P32 table entry outside [0, 4 * num_slots * slot_stride) */
 #define TRTV_DEVERR_BLOCK_IDX 4 /* a top-k block index >= max_pages_per_req */
 #define TRTV_DEVERR_TIMEOUT 8   /* a pipeline wait gave up after 2 s (results invalid) */
 
