@@ -208,3 +208,33 @@ def test_draft_attn_bf16_out_and_split_invariance():
         out = dv.draft().float().cpu().numpy()
         assert np.abs(out - ref).max() <= TOL_BF16, n
     assert T.trtv_get_device_error() == 0
+
+
+def test_draft_attn_graph_replay_with_mutated_lens():
+    """Capture the sub-page view and the drafter attention once; replays with
+    the lengths grown and shrunk on the device match the oracle on the
+    replay's own P32 tables."""
+    p = W.make_problem(kv_lens=[700, 2000, 129], qo_len=1, num_q_heads=32, num_kv_heads=4, head_dim=128,
+                       kv_dtype=W.FP8, seed=66, slot_stride=8, max_pages_per_req=24)
+    dv = DeviceVerify(p, out_dtype="f32")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dv.subpage_view(stream=s)
+        dv.draft(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dv.subpage_view()
+        dv.draft()
+    for lens in ([700, 2000, 129], [3072, 1, 33], [0, 1500, 2048]):
+        lens_t = torch.tensor(lens, dtype=torch.int32)
+        dv.kv_lens.copy_(lens_t)
+        graph.replay()
+        torch.cuda.synchronize()
+        x = oracle.Inputs(p, kv_lens=lens_t)
+        ref, bad = oracle.draft_attn(x, dv.k_sub.cpu().numpy(), dv.v_sub.cpu().numpy())
+        assert np.abs(dv.out.cpu().numpy() - ref).max() <= TOL_FP8
+        err = T.trtv_get_device_error()
+        assert bool(err & T.DEVERR_KV_LEN) == (bad > 0)
