@@ -240,12 +240,13 @@ bool encode_q_map(const trtv_geom* g, const Plan& pl, const void* q, CUtensorMap
 // The tcgen05 attention kernel covers head_dim 128 and a power-of-two group:
 // bf16 caches with 32 < group * qo_len <= 128 rows (one UMMA M = 128 tile;
 // below 33 rows the mma.sync kernel keeps pace with the HBM stream), FP8
-// caches with group * qo_len <= 64 (E4M3 UMMAs read the pages as they are;
-// the lane quadrants without rows host the warps that quantise Q).
+// caches with 16 < group * qo_len <= 64 (E4M3 UMMAs read the pages as they
+// are; the lane quadrants without rows host the warps that quantise Q; a
+// 16-row tile, such as the drafter's decode step, runs faster on mma.sync).
 bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
   if (g->head_dim != 128 || pl.group != pl.group_pad || !aligned(q, 16)) return false;
   const int rows = pl.group * g->qo_len;
-  if (g->kv_dtype == TRTV_FP8_E4M3) return rows <= 64;
+  if (g->kv_dtype == TRTV_FP8_E4M3) return rows > 16 && rows <= 64;
   return rows > 32 && rows <= 128;
 }
 

@@ -132,7 +132,7 @@ def _nan_other_layers(p):
 
 @pytest.mark.parametrize("dtype,Hq,Hk,Tq", [
     (W.BF16, 32, 4, 1),    # drafter decode, 8 rows (mma.sync)
-    (W.FP8, 32, 4, 1),     # FP8 draft layer, 8 rows (tcgen05 E4M3)
+    (W.FP8, 32, 4, 1),     # FP8 draft layer, 8 rows (mma.sync)
     (W.BF16, 64, 4, 4),    # ladder, 64 rows (tcgen05 bf16)
     (W.FP8, 16, 2, 3),     # ladder, 24 -> 32 rows
 ])
