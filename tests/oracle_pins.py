@@ -683,6 +683,23 @@ def check_flat_shrink_across_page_boundary(orc):
     assert not np.array_equal(stale[2:], good[2:])
 
 
+
+def check_flat_counts_clamped(orc):
+    """Row page counts outside [1, max_pages]: a negative or zero length holds
+    no page, a length past the capacity holds max_pages (so later rows keep
+    defined bases); the rebuilt table pads with slot 0 either way."""
+    p = small(seed=45, lens=(5, 600, 300, 1, 256), max_pages_per_req=3)
+    lens = torch.tensor([5, 600, 300, -7, 256], dtype=torch.int32)
+    x = O.Inputs(p, kv_lens=lens)
+    flat, indptr, bad = orc.flatten_page_table(x)
+    assert bad == 2                                     # 600 > 3 * 128, and -7 < qo_len
+    assert list(np.diff(indptr)) == [1, 3, 3, 0, 2]
+    ptn = p.page_table.numpy()
+    assert list(flat[:indptr[-1]]) == [ptn[0, 0], *ptn[1, :3], *ptn[2, :3], *ptn[4, :2]]
+    table, _ = orc.page_table_from_flat(x, flat)
+    assert table[3].tolist() == [0, 0, 0]
+    assert table[4].tolist() == [ptn[4, 0], ptn[4, 1], 0]
+
 # ---------------------------------------------------------------------------
 # drafter attention through the P32 sub-page tables
 

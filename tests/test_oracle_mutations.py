@@ -40,6 +40,7 @@ MUTATIONS = [
     ("flat_floor_pages", [("int64_t n = ((int64_t)L + TRTVO_PAGE - 1) / TRTVO_PAGE;", "int64_t n = (int64_t)L / TRTVO_PAGE;")]),
     ("flat_padding_keeps_entry", [("j < n ? flat[base + j] : 0;", "j < n ? flat[base + j] : flat[base];")]),
     ("flat_rows_at_capacity", [("base += n;", "base += P->max_pages_per_req;")]),
+    ("flat_unclamped", [("return n > P->max_pages_per_req ? P->max_pages_per_req : n;", "return n;")]),
     ("draft_k_from_v_table", [("int64_t ks = k_sub[(int64_t)b * nsub + p / TRTVO_SUBPAGE];",
                                "int64_t ks = v_sub[(int64_t)b * nsub + p / TRTVO_SUBPAGE];")]),
     ("draft_token_rotated", [("int64_t in_sub = ((int64_t)h * TRTVO_SUBPAGE + p % TRTVO_SUBPAGE) * D;",
