@@ -133,3 +133,22 @@ def test_msa_select_argument_checks(lib):
     assert lib.trtv_msa_select(ctypes.byref(g), 16, 16, 16, 16, 2, 0, 16, 256, need, None) == 1
     big = geom(num_q_heads=64, num_kv_heads=2)  # group 32 > 16: no proxy
     assert lib.trtv_msa_select(ctypes.byref(big), 16, 16, 16, 16, 2, 16, 16, 256, 1 << 30, None) == 2
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 on its own,
+    and a C program links every declared entry point against the library."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    calls = "\n".join(f"  p[{i}] = (void (*)(void)){n};" for i, n in enumerate(declared_functions()))
+    src.write_text('#include "trtv.h"\n'
+                   f"int main(void) {{\n  void (*p[{len(declared_functions())}])(void);\n{calls}\n"
+                   "  return p[0] == 0;\n}\n")
+    inc = os.path.join(os.path.dirname(HEADER))
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I" + inc,
+                        str(src), "-o", str(tmp_path / "use"), _build.LIB, "-Wl,-rpath," + os.path.dirname(_build.LIB)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
