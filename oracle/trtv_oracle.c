@@ -38,11 +38,17 @@
  *    times the per-tensor scale;
  *  - a request with kv_len < qo_len, kv_len > 128 * max_pages, or a used page
  *    id outside [0, num_slots) is invalid: its output rows are zero and the
- *    function reports it in its return value.
+ *    function reports it in its return value;
+ *  - the flat (CSR) page table's row b holds ceil(kv_len / 128) pages (0 for
+ *    kv_len <= 0, max_pages past the capacity) from the sum of the earlier
+ *    rows' counts: the row bases come from the lengths;
+ *  - the drafter's attention reads K and V through the P32 tables alone; a
+ *    used entry must lie in [0, 4 * num_slots * slot_stride), the view's
+ *    index scale being the layer-local slot stride.
  *
  * Parity of these definitions with the pages' own implementation is not
  * checkable (the pages hold no code and no vectors); the definitions are
- * pinned by the tests in tests/test_oracle_pins.py.
+ * pinned by the checks in tests/oracle_pins.py (run by test_oracle_pins.py).
  */
 #include <math.h>
 #include <stdint.h>
