@@ -25,8 +25,8 @@ paths      extra workloads (msa and long also timed with trtv_msa_select, the
            decode over an FP8 layer with slot stride 8, read through the P32
            sub-page tables by trtv_draft_attn_p32)
 
---impl reference runs the fp64 oracle as the reference arm (there is no
-runnable reference implementation; see the design notes).
+--impl reference runs the fp64 oracle as the reference arm: the sources of
+the method are text only, so there is no runnable reference implementation.
 Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 """
 from __future__ import annotations

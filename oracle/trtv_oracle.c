@@ -27,7 +27,7 @@
  *             valid-page count, and sparse GQA attention over the selected
  *             blocks.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *  - query head hq uses KV head hq / G, G = Hq / Hk (contiguous GQA groups);
  *  - a proxy block is one 128-token page; its score is the maximum of the
  *    scaled logits over the group's query heads and the in-bound positions of
