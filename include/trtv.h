@@ -81,7 +81,8 @@ typedef enum { TRTV_BF16 = 0, TRTV_FP8_E4M3 = 1, TRTV_F32 = 2 } trtv_dtype;
 #define TRTV_DEVERR_PAGE_ID 2   /* a used page-table entry outside [0, num_slots), or a used
                                    P32 table entry outside [0, 4 * num_slots * slot_stride) */
 #define TRTV_DEVERR_BLOCK_IDX 4 /* a top-k block index >= max_pages_per_req */
-#define TRTV_DEVERR_TIMEOUT 8   /* a pipeline wait gave up after 2 s (results invalid) */
+#define TRTV_DEVERR_TIMEOUT 8   /* a pipeline wait gave up (2 s, or the limit set by
+                                   trtv_test_withhold_pages): that call's results are invalid */
 
 typedef struct {
   int32_t batch;             /* requests B >= 1 */
@@ -323,6 +324,23 @@ trtv_status trtv_draft_attn_p32(const trtv_geom* geom, const void* q, const void
                                 const int32_t* k_sub, const int32_t* v_sub, const int32_t* kv_lens,
                                 void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
                                 void* stream);
+
+/*
+ * Test hook for the bounded waits (the CUDA-graphs commit of "Eagle3 for M3
+ * MSA path + CUDA graphs compatibility" makes the path raise instead of
+ * waiting on state that is not there; here every barrier wait inside a kernel
+ * gives up after a limit, sets TRTV_DEVERR_TIMEOUT and lets the kernel return).
+ *   pages >= 0: until the next call with pages < 0, in the attention and proxy
+ *     kernels launched afterwards (any thread, any device) each CTA's K
+ *     producer stops after `pages` pages, so the waits of its consumers run
+ *     out, and every barrier wait gives up after wait_us microseconds
+ *     (1 .. 2,000,000).  Outputs of those calls are invalid; no wait is left
+ *     unbounded, copies already issued are waited for, TMEM is freed.
+ *   pages < 0: back to normal operation (2 s bound, nothing withheld).
+ * For tests only; not for production use.  TRTV_ERR_INVALID_ARG when wait_us
+ * is out of range.
+ */
+trtv_status trtv_test_withhold_pages(int32_t pages, uint32_t wait_us);
 
 /*
  * Read and clear the current device's error word (TRTV_DEVERR_* bits).

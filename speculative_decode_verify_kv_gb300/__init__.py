@@ -21,7 +21,8 @@ __all__ = [
     "trtv_msa_topk", "trtv_msa_sparse_attn", "trtv_get_device_error", "trtv_version",
     "trtv_verify_dense_noalloc", "trtv_stage_kv", "trtv_flatten_page_table",
     "trtv_page_table_from_flat", "trtv_workspace_bytes_flat", "trtv_verify_dense_flat",
-    "trtv_draft_attn_p32", "trtv_msa_select", "trtv_status_string", "geom_of", "EXPORTS",
+    "trtv_draft_attn_p32", "trtv_msa_select", "trtv_status_string", "trtv_test_withhold_pages",
+    "geom_of", "EXPORTS",
 ]
 
 TRTV_OK, TRTV_ERR_INVALID_ARG, TRTV_ERR_UNSUPPORTED, TRTV_ERR_CUDA, TRTV_ERR_WORKSPACE = range(5)
@@ -33,7 +34,8 @@ EXPORTS = ("trtv_status_string", "trtv_version", "trtv_subpage_view", "trtv_work
            "trtv_verify_dense", "trtv_verify_dense_noalloc", "trtv_msa_proxy_score", "trtv_msa_topk",
            "trtv_msa_sparse_attn", "trtv_stage_kv", "trtv_flatten_page_table",
            "trtv_page_table_from_flat", "trtv_workspace_bytes_flat", "trtv_verify_dense_flat",
-           "trtv_draft_attn_p32", "trtv_msa_select", "trtv_get_device_error")
+           "trtv_draft_attn_p32", "trtv_msa_select", "trtv_test_withhold_pages",
+           "trtv_get_device_error")
 
 
 class TrtvError(RuntimeError):
@@ -108,6 +110,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     h.trtv_msa_select.argtypes = [G, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
     h.trtv_get_device_error.restype = ctypes.c_int
     h.trtv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+    h.trtv_test_withhold_pages.restype = ctypes.c_int
+    h.trtv_test_withhold_pages.argtypes = [i32, ctypes.c_uint32]
     _lib = h
     return h
 
@@ -247,6 +251,13 @@ def trtv_draft_attn_p32(geom: Geom, q, kv_pool, k_sub, v_sub, kv_lens, out, out_
     _check("trtv_draft_attn_p32", load().trtv_draft_attn_p32(
         ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(k_sub), _ptr(v_sub), _ptr(kv_lens),
         _ptr(out), out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_test_withhold_pages(pages: int, wait_us: int = 0) -> None:
+    """Test hook of the bounded waits: K producers stop after ``pages`` pages
+    and every wait gives up after ``wait_us``; ``pages < 0`` restores normal
+    operation."""
+    _check("trtv_test_withhold_pages", load().trtv_test_withhold_pages(pages, wait_us))
 
 
 def trtv_get_device_error(stream=None) -> int:

@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -35,6 +36,9 @@ int* g_err_ptr[kMaxDevices];
 uint8_t* g_noalloc_ptr[kMaxDevices];
 std::set<std::pair<const void*, int>> g_smem_set;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// bounded-wait settings of the next launches (trtv_test_withhold_pages)
+std::atomic<uint64_t> g_wait_ns{kWaitNs};
+std::atomic<int> g_withhold{-1};
 
 int current_device() {
   int d = -1;
@@ -214,7 +218,7 @@ bool plan_attn_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams*
   a->off_scan = static_cast<int>(off);
   off += scan;
   a->off_bar = static_cast<int>(align_up(off, 8));
-  off = a->off_bar + 2 * nst * sizeof(uint64_t);
+  off = a->off_bar + 2 * nst * sizeof(uint64_t) + 8;  // barriers, give-up flag
   a->nstages = nst;
   *bytes = off + kAlignSlack;
   return *bytes <= kSmemOptin;
@@ -350,7 +354,7 @@ bool plan_proxy_smem(const trtv_geom* g, const Plan& pl, ProxyParams* a, size_t*
   a->off_scan = static_cast<int>(off);
   off += scan;
   a->off_bar = static_cast<int>(align_up(off, 8));
-  off = a->off_bar + 2 * nst * sizeof(uint64_t);
+  off = a->off_bar + 2 * nst * sizeof(uint64_t) + 8;  // barriers, give-up flag
   a->nstages = nst;
   *bytes = off + kAlignSlack;
   return *bytes <= kSmemOptin - 1024;
@@ -443,6 +447,8 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   // stream-K charge per sequence start, in pages: what a sequence switch costs
   // each kernel relative to one page of K and V
   a.setup = umma ? kUmmaSeqSetup : kSeqSetup;
+  a.wait_ns = g_wait_ns.load();
+  a.withhold = g_withhold.load();
   cudaError_t e;
   if (rebuilt != nullptr) {
     e = launch_flat_table(false, kvi.flat, lens, g->batch, g->qo_len, g->max_pages_per_req, rebuilt,
@@ -614,6 +620,8 @@ trtv_status proxy_common(const trtv_geom* g, const void* q, const void* kv_pool,
   a.rows_pad = pl.rows_pad;
   a.num_ctas = pl.num_ctas;
   a.score_scale = g->sm_scale * g->k_scale;
+  a.wait_ns = g_wait_ns.load();
+  a.withhold = g_withhold.load();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool fused = select && umma;
   if (fused) {
@@ -730,6 +738,18 @@ trtv_status trtv_draft_attn_p32(const trtv_geom* geom, const void* q, const void
   if (k_sub == nullptr || v_sub == nullptr) return TRTV_ERR_INVALID_ARG;
   return attn_common(geom, q, kv_pool, KvIndex{nullptr, nullptr, k_sub, v_sub}, kv_lens, nullptr, 0,
                      out, out_dtype, workspace, ws_bytes, stream);
+}
+
+trtv_status trtv_test_withhold_pages(int32_t pages, uint32_t wait_us) {
+  if (pages < 0) {
+    g_withhold.store(-1);
+    g_wait_ns.store(kWaitNs);
+    return TRTV_OK;
+  }
+  if (wait_us == 0 || static_cast<uint64_t>(wait_us) * 1000 > kWaitNs) return TRTV_ERR_INVALID_ARG;
+  g_wait_ns.store(static_cast<uint64_t>(wait_us) * 1000);
+  g_withhold.store(pages);
+  return TRTV_OK;
 }
 
 trtv_status trtv_get_device_error(int32_t* host_out, void* stream) {

@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* empty = full + p.nstages;
+  int* abortf = reinterpret_cast<int*>(empty + p.nstages);  // the CTA's give-up flag
+  const Waits wt{p.err, abortf, p.wait_ns};
   int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
   const bool sparse = p.sparse != 0;
   const int Hk = p.num_kv_heads, T = p.qo_len, NST = p.nstages;
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    *abortf = 0;
     fence_mbar_init();
   }
   pdl_wait();  // inputs may come from the previous kernel of the stream
@@ -289,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int st = it % NST;
         const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
-        if (it >= NST && !mbar_wait(&empty[st], ph ^ 1u, p.err)) { alive = false; break; }
+        if (p.withhold >= 0 && it >= p.withhold) { alive = false; break; }  // tests of the give-up path only
+        if (it >= NST && !mbar_wait(&empty[st], ph ^ 1u, wt)) { alive = false; break; }
         const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
                                : static_cast<int>(j);
         const int64_t row = static_cast<int64_t>(cur.b) * p.max_pages + blk;
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // never leave copies in flight: wait for the last issued pages to land
     for (int k = (it > NST ? it - NST : 0); k < it; ++k)
-      mbar_wait(&full[k % NST], static_cast<uint32_t>(k / NST) & 1u, p.err);
+      mbar_drain(&full[k % NST], static_cast<uint32_t>(k / NST) & 1u, wt);
     return;
   }
 
@@ -371,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
         tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
       }
-      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, p.err));
+      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, wt));
       const int pos0 = blk * kPage;
       int bnd[2];
 #pragma unroll

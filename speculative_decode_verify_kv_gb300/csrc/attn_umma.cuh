@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint64_t* qcv = mdone + 1;       // [2]
   uint64_t* qsfree = qcv + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(qsfree + 1);
+  int* abortf = reinterpret_cast<int*>(qsfree + 2);  // the CTA's give-up flag
+  const Waits wt{p.err, abortf, p.wait_ns};
   int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
   // [0,256) merge flags, [256,512) merge row stats, [512,1024) row maxima of
   // the two column halves (double-buffered by page), [1024,1280) row sums
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       mbar_init(&qempty[i], 1);
     }
     mbar_init(mdone, 1);
+    *abortf = 0;
     if constexpr (FP8) {
       for (int i = 0; i < 2; ++i) mbar_init(&qcv[i], 8 - nsoft);
       mbar_init(qsfree, nsoft);
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
         if (!is_v) {
           const int qb = sq % NQ;
-          if (sq >= NQ && !mbar_wait(&qempty[qb], static_cast<uint32_t>(sq / NQ - 1) & 1u, p.err)) {
+          if (sq >= NQ && !mbar_wait(&qempty[qb], static_cast<uint32_t>(sq / NQ - 1) & 1u, wt)) {
             alive = false;
             break;
           }
@@ -246,6 +249,10 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
         const int L = p.sub_k != nullptr ? p.kv_lens[cur.b] : 0;  // P32 tables: used entries
         for (int64_t j = j0; j < j1; ++j, ++it) {
+          if (!is_v && p.withhold >= 0 && it >= p.withhold) {  // tests of the give-up path only
+            alive = false;
+            break;
+          }
           const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
                                  : static_cast<int>(j);
           const int64_t row = static_cast<int64_t>(cur.b) * p.max_pages + blk;
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           }
           const int64_t buf = static_cast<int64_t>(slot) * p.slot_stride + (is_v ? 1 : 0);
           const int st = it % n;
-          if (it >= n && !mbar_wait(&emptyb[st], static_cast<uint32_t>(it / n - 1) & 1u, p.err)) {
+          if (it >= n && !mbar_wait(&emptyb[st], static_cast<uint32_t>(it / n - 1) & 1u, wt)) {
             alive = false;
             break;
           }
@@ -282,9 +289,9 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       }
       // never leave copies in flight
       for (int k = (it > n ? it - n : 0); k < it; ++k)
-        mbar_wait(&fullb[k % n], static_cast<uint32_t>(k / n) & 1u, p.err);
+        mbar_drain(&fullb[k % n], static_cast<uint32_t>(k / n) & 1u, wt);
       if (!is_v && sq >= 1)
-        mbar_wait(&qfull[(sq - 1) % NQ], static_cast<uint32_t>((sq - 1) / NQ) & 1u, p.err);
+        mbar_drain(&qfull[(sq - 1) % NQ], static_cast<uint32_t>((sq - 1) / NQ) & 1u, wt);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- UMMA issuer
@@ -293,8 +300,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       auto issue_pv = [&](int pg, bool first) {
         const int vs = pg % NV, b = pg % kSBufs;
         if (!alive) return;
-        if (!mbar_wait(&vfull[vs], static_cast<uint32_t>(pg / NV) & 1u, p.err) ||
-            !mbar_wait(&pfull[b], static_cast<uint32_t>(pg / kSBufs) & 1u, p.err)) {
+        if (!mbar_wait(&vfull[vs], static_cast<uint32_t>(pg / NV) & 1u, wt) ||
+            !mbar_wait(&pfull[b], static_cast<uint32_t>(pg / kSBufs) & 1u, wt)) {
           alive = false;
           return;
         }
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
            alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
         const int qb = sq % NQ;
-        if (!mbar_wait(FP8 ? &qcv[qb] : &qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err)) {
+        if (!mbar_wait(FP8 ? &qcv[qb] : &qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, wt)) {
           alive = false;
           break;
         }
@@ -334,8 +341,8 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
         for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
           const int ks = it % NK, buf = it % kSBufs;
-          if (!mbar_wait(&kfull[ks], static_cast<uint32_t>(it / NK) & 1u, p.err) ||
-              (it >= kSBufs && !mbar_wait(&pvdone[buf], static_cast<uint32_t>(it / kSBufs - 1) & 1u, p.err))) {
+          if (!mbar_wait(&kfull[ks], static_cast<uint32_t>(it / NK) & 1u, wt) ||
+              (it >= kSBufs && !mbar_wait(&pvdone[buf], static_cast<uint32_t>(it / kSBufs - 1) & 1u, wt))) {
             alive = false;
             break;
           }
@@ -371,7 +378,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         pend = -1;
       }
       umma_commit(mdone);
-      mbar_wait(mdone, 0, p.err);
+      mbar_drain(mdone, 0, wt);
     }
     __syncwarp();
   } else {
@@ -394,9 +401,9 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
            cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
         const int qb = sq % NQ;
         if (!dead)
-          dead = __any_sync(0xffffffffu, !mbar_wait(&qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, p.err));
+          dead = __any_sync(0xffffffffu, !mbar_wait(&qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, wt));
         if (!dead && sq >= 1)
-          dead = __any_sync(0xffffffffu, !mbar_wait(qsfree, static_cast<uint32_t>(sq - 1) & 1u, p.err));
+          dead = __any_sync(0xffffffffu, !mbar_wait(qsfree, static_cast<uint32_t>(sq - 1) & 1u, wt));
         for (int r = ct; r < G * T; r += nct)
           qscale[r] = quantize_q_row(qbase + qb * QBUF, QBUF / 2, qf8, qf8 + kQf8Tile, r);
         fence_proxy_async_smem();
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       float scale = p.scale_log2;
       if constexpr (FP8) {
         if (!dead)
-          dead = __any_sync(0xffffffffu, !mbar_wait(&qcv[sq % NQ], static_cast<uint32_t>(sq / NQ) & 1u, p.err));
+          dead = __any_sync(0xffffffffu, !mbar_wait(&qcv[sq % NQ], static_cast<uint32_t>(sq / NQ) & 1u, wt));
         scale *= valid ? qscale[r] : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(qsfree);
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
           tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
         }
         if (!dead)
-          dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, p.err));
+          dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, wt));
         tc_fence_after();
         const int pos0 = blk * kPage;
         if (live) {
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
             // O must be stable: PV of the previous page has retired
             const int pv = it - 1;
             if (!dead)
-              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[pv % kSBufs], static_cast<uint32_t>(pv / kSBufs) & 1u, p.err));
+              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[pv % kSBufs], static_cast<uint32_t>(pv / kSBufs) & 1u, wt));
             tc_fence_after();
             const float alpha = need ? fast_exp2(m_use - m_new) : 1.f;
             if (need) {
@@ -530,7 +537,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         if (warp == 0 && nvalid < kPage) {
           const int vs = it % NV;
           if (!dead)
-            dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, p.err));
+            dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, wt));
           uint8_t* vst = vring + vs * KV;
           constexpr int NHALF = FP8 ? 1 : 2;  // 128-byte column blocks per token row
           const int nchunks = (kPage - nvalid) * 8 * NHALF;
@@ -548,7 +555,7 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       // ------------------------------------------------------- sequence end
       const int last = it - 1;
       if (!dead)
-        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last % kSBufs], static_cast<uint32_t>(last / kSBufs) & 1u, p.err));
+        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last % kSBufs], static_cast<uint32_t>(last / kSBufs) & 1u, wt));
       tc_fence_after();
       const bool whole = seq_whole(cur, u0, u1, p.setup);
       const int64_t slot = seq_slot(cur, u0, p.setup);

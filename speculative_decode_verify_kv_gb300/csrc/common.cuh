@@ -75,6 +75,11 @@ struct AttnParams {
   const int32_t* sub_k;
   const int32_t* sub_v;
   int num_subpages;
+  // bounded waits: give-up time of every barrier wait, and (tests of that
+  // path only, else -1) the number of pages after which the K producer of
+  // each CTA withholds its loads, so that its consumers' waits run out
+  uint64_t wait_ns;
+  int withhold;
 };
 
 struct ProxyParams {
@@ -96,6 +101,8 @@ struct ProxyParams {
   int32_t* topk_out;
   int32_t* seq_count;
   int topk;
+  uint64_t wait_ns;     // as in AttnParams
+  int withhold;
 };
 
 // ---- small helpers -------------------------------------------------------
@@ -176,15 +183,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, at most kWaitNs.
-// On timeout sets TRTV_DEVERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// Bounded waits of one CTA.  A wait gives up after `limit_ns` (kWaitNs unless
+// a test shortens it): it sets TRTV_DEVERR_TIMEOUT and raises the CTA's abort
+// flag, after which every other wait of the CTA gives up at once, so each role
+// runs out its loops without waiting and all of them meet at the kernel's last
+// barrier.  The loops' barrier counts never depend on whether a wait gave up.
+// Drains -- a producer waiting for the copies it issued, the UMMA issuer for
+// its last instructions -- ignore the flag and keep the full bound: what they
+// wait for was issued and always completes.
+struct Waits {
+  int* err;             // the device error word
+  volatile int* abort;  // shared memory, zeroed before the CTA's first wait
+  uint64_t limit_ns;
+};
+
+// Wait for the phase with the given parity to complete; false when the wait
+// gave up (limit reached, or another wait of the CTA gave up before).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waits& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*w.abort) return false;
+      if (global_timer_ns() - t0 > w.limit_ns) {
+        atomicOr(w.err, TRTV_DEVERR_TIMEOUT);
+        *w.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Wait for work this thread issued (copies in flight, committed UMMAs): not
+// cut short by the abort flag, bounded by kWaitNs.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, const Waits& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitNs) {
-      atomicOr(err, TRTV_DEVERR_TIMEOUT);
+      atomicOr(w.err, TRTV_DEVERR_TIMEOUT);
       return false;
     }
   }

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* empty = full + p.nstages;
+  int* abortf = reinterpret_cast<int*>(empty + p.nstages);  // the CTA's give-up flag
+  const Waits wt{p.err, abortf, p.wait_ns};
   int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
   int32_t* warp_tot = scan + p.batch + 1;
   float* red = reinterpret_cast<float*>(smem + p.off_red);  // [NST][8 slices][32 tokens]
@@ -65,6 +67,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    *abortf = 0;
     fence_mbar_init();
   }
   block_exclusive_scan(p.batch, scan, warp_tot, [&](int i) -> int32_t {
@@ -102,8 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int st = it % NST;
         const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
+        if (p.withhold >= 0 && it >= p.withhold) { alive = false; break; }  // tests of the give-up path only
         if (it >= NST) {
-          const bool ok = mbar_wait(&empty[st], ph ^ 1u, p.err);
+          const bool ok = mbar_wait(&empty[st], ph ^ 1u, wt);
           if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
           flush(st);
         }
@@ -135,9 +139,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = (it > NST ? it - NST : 0); k < it; ++k) {
       const int st = k % NST;
       const bool ok = __all_sync(0xffffffffu,
-                                 mbar_wait(&empty[st], static_cast<uint32_t>(k / NST) & 1u, p.err));
+                                 mbar_wait(&empty[st], static_cast<uint32_t>(k / NST) & 1u, wt));
       if (ok) flush(st);
-      else mbar_wait(&full[st], static_cast<uint32_t>(k / NST) & 1u, p.err);
+      else mbar_drain(&full[st], static_cast<uint32_t>(k / NST) & 1u, wt);
     }
     return;
   }
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t j = j0; j < j1; ++j, ++it) {
       const int st = it % NST;
       const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
-      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, p.err));
+      if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&full[st], ph, wt));
       const int pos0 = static_cast<int>(j) * kPage;
       const uint8_t* kst = smem + p.off_stage + st * p.stage_bytes;
       float rmax[2] = {-INFINITY, -INFINITY};

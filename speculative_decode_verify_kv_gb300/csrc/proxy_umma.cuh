@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
   uint64_t* qempty = qfull + 2;    // [2] UMMAs finished with the Q tile
   uint64_t* mdone = qempty + 2;    // [1] every UMMA retired
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mdone + 1);
+  int* abortf = reinterpret_cast<int*>(tslot + 1);  // the CTA's give-up flag
+  const Waits wt{p.err, abortf, p.wait_ns};
   int32_t* scan = reinterpret_cast<int32_t*>(smem + p.off_scan);
   int32_t* warp_tot = scan + p.batch + 1;
   const int Hk = p.num_kv_heads, T = p.qo_len, NP = p.max_pages, G = p.group;
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
       mbar_init(&qempty[i], 1);
     }
     mbar_init(mdone, 1);
+    *abortf = 0;
     fence_mbar_init();
   }
   block_exclusive_scan(p.batch, scan, warp_tot, [&](int i) -> int32_t {
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
       for (SeqCursor cur = cursor_first(scan, p.batch, Hk, false, u0);
            alive && cur.b < p.batch && cur.start < u1; cursor_next(cur, scan, p.batch, Hk, false), ++sq) {
         const int qb = sq & 1;
-        if (sq >= 2 && !mbar_wait(&qempty[qb], static_cast<uint32_t>((sq >> 1) - 1) & 1u, p.err)) {
+        if (sq >= 2 && !mbar_wait(&qempty[qb], static_cast<uint32_t>((sq >> 1) - 1) & 1u, wt)) {
           alive = false;
           break;
         }
@@ -160,7 +163,8 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
         for (int64_t j = j0; j < j1; ++j, ++it) {
           const int st = it % NST;
           const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
-          if (it >= NST && !mbar_wait(&empty[st], ph ^ 1u, p.err)) { alive = false; break; }
+          if (p.withhold >= 0 && it >= p.withhold) { alive = false; break; }  // tests of the give-up path only
+          if (it >= NST && !mbar_wait(&empty[st], ph ^ 1u, wt)) { alive = false; break; }
           int slot = p.page_table[static_cast<int64_t>(cur.b) * NP + j];
           if (slot < 0 || slot >= p.num_slots) {
             atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
@@ -180,8 +184,8 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
       }
       // never leave copies in flight
       for (int k = (it > NST ? it - NST : 0); k < it; ++k)
-        mbar_wait(&full[k % NST], static_cast<uint32_t>(k / NST) & 1u, p.err);
-      if (sq >= 1) mbar_wait(&qfull[(sq - 1) & 1], static_cast<uint32_t>((sq - 1) >> 1) & 1u, p.err);
+        mbar_drain(&full[k % NST], static_cast<uint32_t>(k / NST) & 1u, wt);
+      if (sq >= 1) mbar_drain(&qfull[(sq - 1) & 1], static_cast<uint32_t>((sq - 1) >> 1) & 1u, wt);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- UMMA issuer
@@ -191,15 +195,15 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
       for (SeqCursor cur = cursor_first(scan, p.batch, Hk, false, u0);
            alive && cur.b < p.batch && cur.start < u1; cursor_next(cur, scan, p.batch, Hk, false), ++sq) {
         const int qb = sq & 1;
-        if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq >> 1) & 1u, p.err)) { alive = false; break; }
+        if (!mbar_wait(&qfull[qb], static_cast<uint32_t>(sq >> 1) & 1u, wt)) { alive = false; break; }
         const uint32_t a0 = smem_u32(qbase + qb * QBUF);
         const int64_t j0 = (u0 > cur.start ? u0 : cur.start) - cur.start;
         const int64_t j1 = ((u1 < cur.start + cur.units) ? u1 : cur.start + cur.units) - cur.start;
         for (int64_t j = j0; j < j1; ++j, ++it) {
           const int st = it % NST, buf = it & 1;
           const uint32_t ph = static_cast<uint32_t>(it / NST) & 1u;
-          if (!mbar_wait(&full[st], ph, p.err)) { alive = false; break; }
-          if (it >= 2 && !mbar_wait(&tempty[buf], static_cast<uint32_t>((it >> 1) - 1) & 1u, p.err)) {
+          if (!mbar_wait(&full[st], ph, wt)) { alive = false; break; }
+          if (it >= 2 && !mbar_wait(&tempty[buf], static_cast<uint32_t>((it >> 1) - 1) & 1u, wt)) {
             alive = false;
             break;
           }
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
         umma_commit(&qempty[qb]);
       }
       umma_commit(mdone);
-      mbar_wait(mdone, 0, p.err);
+      mbar_drain(mdone, 0, wt);
     }
     __syncwarp();
   } else {
@@ -239,7 +243,7 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int buf = it & 1;
         if (buf != wg) continue;
-        if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&tfull[buf], static_cast<uint32_t>(it >> 1) & 1u, p.err));
+        if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&tfull[buf], static_cast<uint32_t>(it >> 1) & 1u, wt));
         tc_fence_after();
         float m = -INFINITY;
         if (warp_live) {
