@@ -18,7 +18,7 @@ LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libtrtv.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["abi.cu", "small_kernels.cu", "attn_bf16.cu", "attn_fp8.cu", "proxy_bf16.cu",
+SOURCES = ["abi.cu", "small_kernels.cu", "attn_bf16.cu", "attn_fp8.cu", "attn_pm.cu", "proxy_bf16.cu",
            "proxy_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",

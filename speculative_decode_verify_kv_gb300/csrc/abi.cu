@@ -241,16 +241,16 @@ bool encode_q_map(const trtv_geom* g, const Plan& pl, const void* q, CUtensorMap
   return r == CUDA_SUCCESS;
 }
 
-// The tcgen05 attention kernel covers head_dim 128 and a power-of-two group:
-// bf16 caches with 32 < group * qo_len <= 128 rows (one UMMA M = 128 tile;
-// below 33 rows the mma.sync kernel keeps pace with the HBM stream), FP8
-// caches with 16 < group * qo_len <= 64 (E4M3 UMMAs read the pages as they
-// are; the lane quadrants without rows host the warps that quantise Q; a
-// 16-row tile, such as the drafter's decode step, runs faster on mma.sync).
+// The row-major tcgen05 attention kernel covers head_dim 128 and a
+// power-of-two group: bf16 caches with 32 < group * qo_len <= 128 rows (one
+// UMMA M = 128 tile; below 33 rows the mma.sync kernel keeps pace with the
+// HBM stream), FP8 caches with 32 < group * qo_len <= 64 (E4M3 UMMAs read the
+// pages as they are; the lane quadrants without rows host the warps that
+// quantise Q; tiles of at most 32 rows go to the position-major kernel).
 bool attn_umma_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
   if (g->head_dim != 128 || pl.group != pl.group_pad || !aligned(q, 16)) return false;
   const int rows = pl.group * g->qo_len;
-  if (g->kv_dtype == TRTV_FP8_E4M3) return rows > 16 && rows <= 64;
+  if (g->kv_dtype == TRTV_FP8_E4M3) return rows > 32 && rows <= 64;
   return rows > 32 && rows <= 128;
 }
 
@@ -291,6 +291,69 @@ bool plan_attn_umma_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnPa
     a->nstages = nk;
     a->nv = nv;
     a->nq = nq;
+    a->qbuf = static_cast<int>(qbuf);
+    a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
+    *bytes = off + kAlignSlack;
+    if (*bytes <= kSmemOptin) return true;
+  }
+  return false;
+}
+
+// The position-major tcgen05 kernel (positions on the UMMA's M, rows on N)
+// covers FP8 caches with head_dim 128 and a power-of-two group with at most 32
+// rows (group * qo_len): the FP8 verify and drafter tiles, where rows as M
+// would leave most of each instruction idle.  (Its bf16 form keeps up with the
+// HBM stream too, but racing ahead of the mma.sync kernel's pace it leaves
+// some SMs with less bandwidth and a longer tail, so bf16 tiles of at most 32
+// rows stay on the mma.sync kernel.)
+bool attn_pm_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
+  return g->kv_dtype == TRTV_FP8_E4M3 && g->head_dim == 128 && pl.group == pl.group_pad && aligned(q, 16) &&
+         pl.group * g->qo_len <= 32;
+}
+
+// Shared memory of the position-major kernel: Q tiles (bf16, two 64-column
+// halves of rows_pad rows), FP8: two sequences' E4M3 Q terms, the 16 KB P^T
+// region, the K and V rings; as deep as fits, two Q tiles preferred.
+bool plan_attn_pm_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
+  const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
+  const int nr = pl.rows_pad;
+  const size_t qbuf = static_cast<size_t>(2) * nr * 128;
+  const size_t qf8 = fp8 ? static_cast<size_t>(2) * 2 * nr * 128 : 0;
+  const size_t preg = 128 * 128;
+  const size_t kv = fp8 ? static_cast<size_t>(kGroups) * kBox : static_cast<size_t>(kGroups) * 2 * kBox;
+  const int nitems = sparse ? pl.n_seq : g->batch;
+  const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
+  const size_t ml = static_cast<size_t>(8 + 4 + 2) * nr * sizeof(float) + 8 * sizeof(int);  // + vote slots
+  const int np = 128 / (2 * nr);
+  struct Depth { int nq, nk, nv; };
+  static const Depth kBf16[] = {{2, 3, 3}, {1, 3, 3}, {2, 3, 2}, {2, 2, 2}};
+  static const Depth kFp8[] = {{2, 6, 6}, {2, 6, 5}, {2, 5, 5}, {2, 4, 4}, {2, 3, 3}, {2, 2, 2}};
+  const Depth* list = fp8 ? kFp8 : kBf16;
+  const int nlist = fp8 ? 6 : 4;
+  for (int i = 0; i < nlist; ++i) {
+    const Depth d = list[i];
+    size_t off = 0;
+    a->off_q = 0;
+    off += d.nq * qbuf;
+    a->off_qf8 = static_cast<int>(off);
+    off += qf8;
+    a->off_p = static_cast<int>(off);
+    off += preg;
+    a->off_stage = static_cast<int>(off);
+    a->stage_bytes = static_cast<int>(kv);
+    off += d.nk * kv;
+    a->off_vring = static_cast<int>(off);
+    off += d.nv * kv;
+    a->off_scan = static_cast<int>(off);
+    off += scan;
+    a->off_ml = static_cast<int>(align_up(off, 16));
+    off = a->off_ml + ml;
+    a->off_bar = static_cast<int>(align_up(off, 8));
+    off = a->off_bar + (2 * d.nk + 2 * d.nv + 2 * np + 16) * sizeof(uint64_t) + 16;
+    a->nstages = d.nk;
+    a->nv = d.nv;
+    a->nq = d.nq;
+    a->np = np;
     a->qbuf = static_cast<int>(qbuf);
     a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
     *bytes = off + kAlignSlack;
@@ -402,12 +465,14 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   if (err == nullptr) return TRTV_ERR_CUDA;
   AttnParams a{};
   size_t smem = 0;
-  const bool umma = attn_umma_eligible(g, pl, q);
-  if (umma ? !plan_attn_umma_smem(g, pl, sparse, &a, &smem) : !plan_attn_smem(g, pl, sparse, &a, &smem))
+  const bool pm = attn_pm_eligible(g, pl, q);
+  const bool umma = !pm && attn_umma_eligible(g, pl, q);
+  if (pm ? !plan_attn_pm_smem(g, pl, sparse, &a, &smem)
+         : umma ? !plan_attn_umma_smem(g, pl, sparse, &a, &smem) : !plan_attn_smem(g, pl, sparse, &a, &smem))
     return TRTV_ERR_UNSUPPORTED;
   CUtensorMap map, qmap;
   if (!encode_pool_map(g, pl, pool, &map)) return TRTV_ERR_CUDA;
-  if (umma && !encode_q_map(g, pl, q, &qmap)) return TRTV_ERR_CUDA;
+  if ((pm || umma) && !encode_q_map(g, pl, q, &qmap)) return TRTV_ERR_CUDA;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -446,7 +511,9 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   a.v_scale = g->v_scale;
   // stream-K charge per sequence start, in pages: what a sequence switch costs
   // each kernel relative to one page of K and V
-  a.setup = umma ? kUmmaSeqSetup : kSeqSetup;
+  a.setup = (pm || umma) ? kUmmaSeqSetup : kSeqSetup;
+  a.lg_group = 0;
+  while ((1 << a.lg_group) < pl.group) ++a.lg_group;
   a.wait_ns = g_wait_ns.load();
   a.withhold = g_withhold.load();
   cudaError_t e;
@@ -463,7 +530,8 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
                            reinterpret_cast<int32_t*>(wsb + pl.ws_count), err, st);
     if (e != cudaSuccess) return TRTV_ERR_CUDA;
   }
-  e = umma ? (g->kv_dtype == TRTV_FP8_E4M3 ? launch_attn_umma_fp8(map, qmap, a, pl.num_ctas, smem, st)
+  e = pm     ? launch_attn_pm(g->kv_dtype == TRTV_FP8_E4M3, pl.rows_pad, map, qmap, a, pl.num_ctas, smem, st)
+      : umma ? (g->kv_dtype == TRTV_FP8_E4M3 ? launch_attn_umma_fp8(map, qmap, a, pl.num_ctas, smem, st)
                                            : launch_attn_umma(map, qmap, a, pl.num_ctas, smem, st))
        : g->kv_dtype == TRTV_FP8_E4M3
            ? launch_attn_fp8(g->head_dim, pl.mt, map, a, pl.num_ctas, smem, st)

@@ -25,9 +25,15 @@ cudaError_t launch_attn_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map
                              int grid, size_t smem, cudaStream_t st);
 
 // tcgen05 attention over FP8 E4M3 caches: head_dim 128, power-of-two group,
-// group * qo_len <= 64 (kind::f8f6f4 UMMAs; Q and P rounded to E4M3)
+// 32 < group * qo_len <= 64 (kind::f8f6f4 UMMAs; Q and P as two E4M3 terms)
 cudaError_t launch_attn_umma_fp8(const CUtensorMap& kv_map, const CUtensorMap& q_map, const AttnParams& p,
                                  int grid, size_t smem, cudaStream_t st);
+
+// position-major tcgen05 attention (positions on the UMMA's M, rows on N):
+// FP8 caches, head_dim 128, power-of-two group, group * qo_len <= nr rows,
+// nr in {16, 32}
+cudaError_t launch_attn_pm(bool fp8, int nr, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                           const AttnParams& p, int grid, size_t smem, cudaStream_t st);
 
 // tcgen05 proxy: bf16, head_dim 128, power-of-two group <= 16, group * qo_len <= 128
 cudaError_t launch_proxy_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const ProxyParams& p,

@@ -452,6 +452,54 @@ def test_msa_pipeline_fp8():
     assert np.array_equal(idx, ref_idx)
 
 
+@pytest.mark.parametrize("Hq,Hk,Tq,num_ctas", [(32, 4, 4, 0), (32, 4, 4, 7), (16, 4, 4, 3), (8, 8, 2, 0)])
+def test_sparse_fp8_small_tiles(Hq, Hk, Tq, num_ctas):
+    """FP8 sparse attention on tiles of at most 32 rows (the position-major
+    tensor-core kernel: 32, 16 and 2 rows), on the GPU's own selection and on
+    the full selection (= dense)."""
+    p = W.make_problem(kv_lens=[3000, 129, Tq, 1500, 700], qo_len=Tq, num_q_heads=Hq, num_kv_heads=Hk,
+                       head_dim=128, kv_dtype=W.FP8, seed=Hq + Tq + num_ctas, topk=6, max_pages_per_req=24,
+                       slack_slots=3)
+    dv = DeviceVerify(p, num_ctas=num_ctas, out_dtype="f32")
+    out = dv.msa().cpu().numpy()
+    idx = dv.block_idx.cpu().numpy()
+    x = oracle.Inputs(p)
+    ref, bad = oracle.sparse_attn(x, idx)
+    assert bad == 0
+    assert np.abs(out - ref).max() <= TOL_FP8
+    npg = torch.tensor([(int(L) + 127) // 128 for L in p.kv_lens])
+    full = torch.arange(24, dtype=torch.int32).view(1, 1, 1, 24).expand(p.batch, Tq, Hk, 24)
+    full = torch.where(full < npg.view(-1, 1, 1, 1), full, torch.full_like(full, -1)).contiguous()
+    dv24 = DeviceVerify(p, num_ctas=num_ctas, out_dtype="f32", topk=24)  # workspace for 24-block lists
+    out2 = dv24.sparse(block_idx=full.cuda(), topk=24).cpu().numpy()
+    dense_ref, _ = oracle.verify_dense(x)
+    assert np.abs(out2 - dense_ref).max() <= TOL_FP8
+    assert T.trtv_get_device_error() == 0
+
+
+def test_fp8_graph_replay_with_mutated_lens():
+    """FP8 cache, 32-row tiles: capture once, replay with kv_lens changed on the device."""
+    full = W.make_problem(kv_lens=[2048, 2048, 2048, 2048], qo_len=4, num_q_heads=32, num_kv_heads=4,
+                          head_dim=128, kv_dtype=W.FP8, seed=88, max_pages_per_req=16)
+    dv = DeviceVerify(full, out_dtype="f32")
+    s = torch.cuda.Stream()
+    dv.kv_lens.copy_(torch.tensor([200, 900, 50, 1400], dtype=torch.int32))
+    with torch.cuda.stream(s):
+        dv.dense(stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dv.dense(stream=s)
+    for lens in ([200, 900, 50, 1400], [2048, 5, 1300, 1401], [4, 4, 2047, 700]):
+        lt = torch.tensor(lens, dtype=torch.int32)
+        dv.kv_lens.copy_(lt)
+        g.replay()
+        torch.cuda.synchronize()
+        ref, _ = oracle.verify_dense(oracle.Inputs(full, kv_lens=lt))
+        assert np.abs(dv.out.cpu().numpy() - ref).max() <= TOL_FP8, lens
+    assert T.trtv_get_device_error() == 0
+
+
 # ---------------------------------------------------------------------------
 # KV slot staging along the ladder (bit-exact against the oracle)
 
