@@ -4,26 +4,23 @@ Headline workload ("dense"): batch 64, qo_len 4, kv_len ~ U{1024..8192},
 32 query / 4 KV heads, head_dim 128, bf16 K/V in P128 pages read through the
 P32 grouped-HND view, bf16 output.  One step = one verify pass of that batch:
 the P32 sub-page view (trtv_subpage_view) and the dense ladder attention with
-its split-KV merge (trtv_verify_dense).  The MSA sparse pass (proxy scores
--> per-token top-k -> sparse attention) is timed the same way on the "msa"
-workload (batch 32, kv_len ~ U{16384..65536}, 64 / 4 heads, top-k 16) and
-reported under "paths".
+its split-KV merge (trtv_verify_dense).  The other workloads are timed the
+same way and printed first, one short JSON line each ("path": msa, fp8, long,
+draft), with the KV slot staging and flat-table lines; the headline line is
+printed last.
 
-value      query tokens per second (batch * qo_len per step), whole job
+value      query tokens per second (batch * qo_len per step), whole job;
+           ms_per_step is the median of repeats of the K-step loop (repeated
+           until about a second is timed, so clock samples fall inside it)
 e2e        the same through the C ABI with per-step host->device copies of
            q / page table / kv_lens from pinned memory and the output read back
 roofline   the dominant call (trtv_verify_dense: the attention kernel and its
-           split-combine kernel) against the measured HBM copy bandwidth;
-           algorithmic bytes = K and V of every visible position + Q + O
+           split-combine kernel) timed as the step is, K calls back to back
+           with events around the loop (its time is its share of the step),
+           against the measured HBM copy bandwidth (also given as a fraction
+           of the nominal 8 TB/s); algorithmic bytes = K and V of every
+           visible position + Q + O
 cpu_baseline  the fp64 oracle on a bounded sample of the same workload
-stage_kv   trtv_stage_kv (the verify tokens' K/V written into their slots),
-           timed on its own copy of the pool, outside the step
-flat_table the flat (CSR) page-table calls on the headline workload: restaging
-           the flat table, and the dense verify taking it
-paths      extra workloads (msa and long also timed with trtv_msa_select, the
-           top-k fused into the proxy kernel): msa, fp8, long, and draft (the drafter's qo_len-1
-           decode over an FP8 layer with slot stride 8, read through the P32
-           sub-page tables by trtv_draft_attn_p32)
 
 --impl reference runs the fp64 oracle as the reference arm: the sources of
 the method are text only, so there is no runnable reference implementation.
@@ -48,7 +45,7 @@ sys.path.insert(0, ROOT)
 METRIC = "verify query-tokens/s and KV HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "query-tokens/s"
 L2_BYTES = 129 * 1024 * 1024
-NOMINAL_HBM_GBS = 7900.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal ("~8 TB/s")
 
 
 def peaks():
@@ -210,67 +207,107 @@ def describe(p, name):
             "seed": 1000 + ["tiny", "dense", "msa", "fp8", "long", "draft"].index(name)}
 
 
-def time_path(name, steps, warmup, sampler=None):
-    """Device-time `steps` verify passes of workload `name` (inputs resident in
-    HBM): once with events only around the whole loop (the step time; nothing
-    between the calls, so each kernel's programmatic dependent launch can
-    overlap the previous one), then again with an event after every call (the
-    per-call times)."""
+def dominant_call(p, name):
+    """The call whose kernels dominate a step of workload `name`."""
+    return "proxy" if p.topk else ("draft_attn" if name == "draft" else "verify_dense")
+
+
+def dominant_bytes(p, name) -> int:
+    return proxy_bytes(p) if p.topk else dense_bytes(p)
+
+
+def config_of(p, name, world):
+    """The bench line's config (the same dict for both arms)."""
+    kv = dominant_bytes(p, name)
+    return dict(describe(p, name),
+                l2=f"inputs larger than L2: {kv / 2**20:.0f} MiB of KV read per step vs "
+                   f"{L2_BYTES / 2**20:.0f} MiB L2, no flush",
+                parallelism="replicas" if world > 1 else "single GPU")
+
+
+def _calls(dv, p, name):
+    msa = p.topk > 0
+    if msa:
+        # proxy, top-k, sparse plan, attention, split combine
+        return [("proxy", dv.proxy), ("topk", dv.select), ("sparse", dv.sparse)], 5
+    if name == "draft":
+        # sub-page view, attention through the P32 tables, split combine
+        return [("subpage_view", dv.subpage_view), ("draft_attn", dv.draft)], 3
+    return [("subpage_view", dv.subpage_view), ("verify_dense", dv.dense)], 3
+
+
+def time_path(name, steps, warmup, sampler=None, min_seconds=1.0, max_repeats=20, dist=None):
+    """Device-time verify passes of workload `name` (inputs resident in HBM).
+
+    Step: every call of a step goes out back to back (each kernel's
+    programmatic dependent launch may overlap the previous one) with events
+    only around the K-step loop, which is repeated until `min_seconds` of
+    device time (at least once); ms_per_step is the median repeat.  Dominant
+    call: the same K-step loop with that call alone (events around the loop),
+    so its time is the call's own share of a step.  Per-call times of every
+    call come from a third, shorter loop with an event after every call."""
     import torch
     from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
     p = make(name)
     dv = DeviceVerify(p)
-    msa = p.topk > 0
-    draft = name == "draft"
-    if msa:
-        calls = [("proxy", dv.proxy), ("topk", dv.select), ("sparse", dv.sparse)]
-        launches = 5   # proxy, top-k, sparse plan, attention, split combine
-    elif draft:
-        calls = [("subpage_view", dv.subpage_view), ("draft_attn", dv.draft)]
-        launches = 3   # sub-page view, attention through the P32 tables, split combine
-    else:
-        calls = [("subpage_view", dv.subpage_view), ("verify_dense", dv.dense)]
-        launches = 3   # sub-page view, attention, split combine
+    calls, launches = _calls(dv, p, name)
+    dom = dominant_call(p, name)
+    dom_f = dict(calls)[dom]
     for _ in range(warmup):
         for _, f in calls:
             f()
     torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    torch.cuda.synchronize()
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def loop(fs):
+        a, b = E(), E()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            for f in fs:
+                f()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    reps = []
     t0 = time.time()
-    start.record()
-    for k in range(steps):
-        for _, f in calls:
-            f()
-    end.record()
-    torch.cuda.synchronize()
+    total = 0.0
+    while (total < min_seconds * 1e3 and len(reps) < max_repeats) or not reps:
+        ms = loop([f for _, f in calls])
+        total += ms
+        reps.append(ms / steps)
     t1 = time.time()
-    total_ms = start.elapsed_time(end)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
-    for k in range(steps):
+    dom_reps = [loop([dom_f]) / steps for _ in range(3)]
+    n_pc = max(10, steps // 8)
+    ev = [[E() for _ in range(len(calls) + 1)] for _ in range(n_pc)]
+    for k in range(n_pc):
         e = ev[k]
         e[0].record()
         for i, (_, f) in enumerate(calls):
             f()
             e[i + 1].record()
     torch.cuda.synchronize()
-    per_call = {}
-    for i, (n, _) in enumerate(calls):
-        per_call[n] = float(np.mean([ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps)]))
+    per_call = {n: float(np.mean([ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(n_pc)]))
+                for i, (n, _) in enumerate(calls)}
     from speculative_decode_verify_kv_gb300 import trtv_get_device_error
     derr = trtv_get_device_error()
-    res = {"p": p, "dv": dv, "ms_per_step": total_ms / steps, "per_call_ms": per_call,
+    res = {"p": p, "dv": dv, "ms_per_step": float(np.median(reps)), "repeats": len(reps),
+           "timed_s": total / 1e3, "dom": dom, "dom_ms": float(np.median(dom_reps)), "per_call_ms": per_call,
            "t0": t0, "t1": t1, "launches_per_step": launches, "device_error": derr}
-    if msa:
+    if p.topk:
         idx = dv.block_idx.cpu().numpy()
         sb, umean = sparse_bytes(p, idx)
-        res["bytes"] = {"proxy": proxy_bytes(p), "sparse": sb, "topk": p.batch * p.qo_len * p.num_kv_heads * (p.max_pages_per_req * 4 + p.topk * 4)}
+        res["bytes"] = {"proxy": proxy_bytes(p), "sparse": sb,
+                        "topk": p.batch * p.qo_len * p.num_kv_heads * (p.max_pages_per_req * 4 + p.topk * 4)}
         res["unique_blocks_mean"] = umean
     else:
-        res["bytes"] = {"draft_attn" if draft else "verify_dense": dense_bytes(p),
+        res["bytes"] = {dom: dense_bytes(p),
                         "subpage_view": p.batch * p.max_pages_per_req * (4 + 32) + p.batch * 4}
     return res
 
@@ -489,7 +526,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": describe(p, args.workload),
+            "config": config_of(p, args.workload, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle",
                              "sample": f"{per} requests per step of the {args.workload} workload"},
@@ -536,78 +573,109 @@ def main():
     T.trtv_get_device_error()
 
     sampler = ClockSampler(local)
+    peak, peak_kind = peaks()
+
+    def sig(x, n=4):
+        return float(f"{x:.{n}g}")
+
+    def path_line(name, r):
+        """One short JSON line per workload: step, per-call and dominant times."""
+        pe = r["p"]
+        step_bytes = sum(r["bytes"].values())
+        gbs = step_bytes / (r["ms_per_step"] / 1e3) / 1e9
+        calls = {}
+        for n, b in r["bytes"].items():
+            ms_c = r["per_call_ms"][n]
+            g = b / (ms_c / 1e3) / 1e9
+            calls[n] = [sig(ms_c * 1e3), sig(g), sig(g / peak, 3)]
+        dg = r["bytes"][r["dom"]] / (r["dom_ms"] / 1e3) / 1e9
+        return {"path": name, "workload": describe(pe, name)["workload"],
+                "value": sig(pe.batch * pe.qo_len / (r["ms_per_step"] / 1e3)), "unit": UNIT,
+                "ms_per_step": sig(r["ms_per_step"]), "repeats": r["repeats"],
+                "step_gbs": sig(gbs), "step_frac_of_measured": sig(gbs / peak, 3),
+                "step_frac_of_8tbs": sig(gbs / NOMINAL_HBM_GBS, 3),
+                "dominant": {"call": r["dom"], "us_alone": sig(r["dom_ms"] * 1e3), "gbs": sig(dg),
+                             "frac_of_measured": sig(dg / peak, 3), "frac_of_8tbs": sig(dg / NOMINAL_HBM_GBS, 3)},
+                "calls_us_gbs_frac": calls, "device_error": r["device_error"],
+                "gpu_launches_per_step": r["launches_per_step"]}
+
+    # ---- other workloads first (one short line each), then the headline
+    summary = {}
+    for extra in [w for w in args.paths.split(",") if w and w not in (args.workload, "none")]:
+        r = time_path(extra, max(10, args.steps // 8), args.warmup, min_seconds=0.3, dist=dist)
+        pl = path_line(extra, r)
+        if "unique_blocks_mean" in r:
+            pl["unique_blocks_mean"] = sig(r["unique_blocks_mean"])
+        if r["p"].topk:
+            f = time_msa_fused(extra, max(10, args.steps // 8), args.warmup)
+            pl["fused_select"] = {"step_us": sig(f["step_ms"] * 1e3), "select_us": sig(f["select_ms"] * 1e3),
+                                  "device_error": f["device_error"]}
+        else:
+            st = time_stage(extra, max(10, args.steps // 8), args.warmup)
+            pl["stage_kv"] = {"us": sig(st["ms"] * 1e3), "bytes": st["bytes"], "gbs": sig(st["gbs"])}
+        summary[extra] = {"value": pl["value"], "ms_per_step": pl["ms_per_step"],
+                          "dominant_frac_of_measured": pl["dominant"]["frac_of_measured"]}
+        if rank == 0:
+            print(json.dumps(pl), flush=True)
+        del r
+        _CACHE.pop(extra, None)
+        torch.cuda.empty_cache()
+
     if dist:
         dist.barrier()
-    head = time_path(args.workload, args.steps, args.warmup, sampler)
+    head = time_path(args.workload, args.steps, args.warmup, sampler, dist=dist)
     sampler.stop()
     clocks = sampler.summary(head["t0"], head["t1"])
     ms = max_over_ranks(head["ms_per_step"], dist)
     p = head["p"]
     qtok = p.batch * p.qo_len
     value = job_value(qtok, world, ms)
+    if rank == 0:
+        print(json.dumps(path_line(args.workload, head)), flush=True)
 
-    peak, peak_kind = peaks()
-    dom = "proxy" if p.topk else ("draft_attn" if args.workload == "draft" else "verify_dense")
-    dom_ms = head["per_call_ms"][dom]
+    dom = head["dom"]
+    dom_ms = head["dom_ms"]
     dom_bytes = head["bytes"][dom]
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     step_bytes = sum(head["bytes"].values())
     kernel_name = ("proxy_umma_kernel" if p.topk else
                    "attn_kernel; the timed call also holds the split-combine kernel")
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": ncu_traffic(dom, args.workload),
+    roofline = {"bound": "hbm", "achieved": sig(achieved), "peak": peak, "unit": "GB/s",
+                "frac": sig(achieved / peak, 4), "traffic": ncu_traffic(dom, args.workload),
                 "kernel": f"{dom} ({kernel_name})", "peak_kind": f"of {peak_kind}",
-                "algorithmic_bytes": dom_bytes, "launch_ms": dom_ms,
-                "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS}
-
-    paths = {}
-    for extra in [w for w in args.paths.split(",") if w and w not in (args.workload, "none")]:
-        r = time_path(extra, max(10, args.steps // 8), args.warmup)
-        pe = r["p"]
-        per = {}
-        for n, b in r["bytes"].items():
-            per[n] = {"ms": r["per_call_ms"][n], "bytes": b,
-                      "gbs": b / (r["per_call_ms"][n] / 1e3) / 1e9,
-                      "frac": b / (r["per_call_ms"][n] / 1e3) / 1e9 / peak}
-        pv = {"config": describe(pe, extra), "ms_per_step": r["ms_per_step"],
-              "value": pe.batch * pe.qo_len / (r["ms_per_step"] / 1e3), "unit": UNIT,
-              "step_gbs": sum(r["bytes"].values()) / (r["ms_per_step"] / 1e3) / 1e9,
-              "calls": per, "device_error": r["device_error"],
-              "gpu_launches_per_step": r["launches_per_step"]}
-        if "unique_blocks_mean" in r:
-            pv["unique_blocks_mean"] = r["unique_blocks_mean"]
-        if not pe.topk:
-            pv["stage_kv"] = time_stage(extra, max(10, args.steps // 8), args.warmup)
-        else:
-            pv["fused_select"] = time_msa_fused(extra, max(10, args.steps // 8), args.warmup)
-        paths[extra] = pv
-        del r
-        _CACHE.pop(extra, None)
-        torch.cuda.empty_cache()
+                "algorithmic_bytes": dom_bytes, "launch_ms": sig(dom_ms),
+                "frac_of_nominal_8tbs": sig(achieved / NOMINAL_HBM_GBS, 4)}
 
     stage = time_stage(args.workload, max(10, args.steps // 8), args.warmup)
-    flat = None if p.topk else time_flat(args.workload, max(10, args.steps // 8), args.warmup)
+    if rank == 0:
+        print(json.dumps({"aux": "stage_kv", "workload": args.workload, "us": sig(stage["ms"] * 1e3),
+                          "bytes": stage["bytes"], "gbs": sig(stage["gbs"]), "launches_per_call": 1}), flush=True)
+    if not p.topk:
+        flat = time_flat(args.workload, max(10, args.steps // 8), args.warmup)
+        if rank == 0:
+            print(json.dumps({"aux": "flat_table", "workload": args.workload,
+                              "flatten_us": sig(flat["flatten_ms"] * 1e3),
+                              "verify_dense_flat_us": sig(flat["verify_dense_flat_ms"] * 1e3),
+                              "verify_dense_us": sig(flat["verify_dense_ms"] * 1e3),
+                              "launches": flat["launches"]}), flush=True)
 
     e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)
     if dist and e2e:
         e2e["value"] = job_value(qtok, world, max_over_ranks(e2e["ms_per_step"], dist))
 
+    gbs = step_bytes / (ms / 1e3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms, "repeats": head["repeats"],
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": p.kv_dtype.replace("fp8_e4m3", "fp8e4m3"),
-            "data": "synthetic",
-            "config": dict(describe(p, args.workload),
-                           l2=f"inputs larger than L2: {dom_bytes / 2**20:.0f} MiB of KV read per "
-                              f"step vs {L2_BYTES / 2**20:.0f} MiB L2, no flush",
-                           parallelism="replicas" if world > 1 else "single GPU"),
-            "kv_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,
-            "kv_hbm_pct_of_measured_peak": 100 * step_bytes / (ms / 1e3) / 1e9 / peak,
-            "per_call_ms": head["per_call_ms"], "roofline": roofline,
+            "data": "synthetic", "config": config_of(p, args.workload, world),
+            "kv_hbm_gbs": sig(gbs), "kv_hbm_pct_of_measured_peak": sig(100 * gbs / peak),
+            "kv_hbm_pct_of_nominal_8tbs": sig(100 * gbs / NOMINAL_HBM_GBS),
+            "per_call_ms": {k: sig(v) for k, v in head["per_call_ms"].items()}, "roofline": roofline,
             "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
                     if e2e else None),
-            "gpu_launches": head["launches_per_step"] * args.steps, "clocks": clocks,
-            "device_error": head["device_error"], "paths": paths, "stage_kv": stage,
-            "flat_table": flat}
+            "gpu_launches": head["launches_per_step"] * args.steps * head["repeats"],
+            "clocks": clocks, "device_error": head["device_error"], "paths": summary}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:

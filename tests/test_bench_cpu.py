@@ -59,3 +59,5 @@ def test_reference_arm_line():
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the same config dict as the GPU arm prints for this workload
+    assert line["config"] == bench.config_of(bench.make("tiny"), "tiny", 1)

@@ -1,8 +1,9 @@
 """trtv_verify_dense_noalloc: the dense verify entry point for callers that
 cannot allocate device memory (its scratch is a static device array inside the
 library).  Its output must match trtv_verify_dense with a caller workspace on
-two calls in a row.  This file is collected last, so a run that stops at the
-first failure has already run every other test."""
+calls in a row, and the calls must leave the device's free memory unchanged.
+This file is collected last, so a run that stops at the first failure has
+already run every other test."""
 import pytest
 import torch
 
@@ -33,12 +34,17 @@ def test_noalloc_matches_workspace_entry_point(lens, Hq, Hk, D):
                        seed=len(lens) + D, slack_slots=5)
     dv = DeviceVerify(p, out_dtype="f32")
     ref = dv.dense().clone()
-    for _ in range(2):
-        out = torch.full_like(dv.out, float("nan"))
+    outs = [torch.full_like(dv.out, float("nan")) for _ in range(3)]
+    torch.cuda.synchronize()
+    free = []
+    for out in outs:
         T.trtv_verify_dense_noalloc(dv.geom, dv.q, dv.pool, dv.page_table, dv.kv_lens, out, T.TRTV_F32)
         torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
         assert torch.isfinite(out).all()
         assert (out - ref).abs().max().item() <= TOL
+    # the entry point allocates nothing: device memory stays as it was after the first call
+    assert free[1] == free[0] and free[2] == free[0], free
     assert T.trtv_get_device_error() == 0
 
 
