@@ -312,24 +312,24 @@ bool attn_pm_eligible(const trtv_geom* g, const Plan& pl, const void* q) {
 }
 
 // Shared memory of the position-major kernel: Q tiles (bf16, two 64-column
-// halves of rows_pad rows), FP8: two sequences' E4M3 Q terms, the 16 KB P^T
-// region, the K and V rings; as deep as fits, two Q tiles preferred.
+// halves of rows_pad rows), FP8: two sequences' E4M3 Q terms, the P^T regions
+// (four buffers of 2 rows_pad bytes per 128-byte row), the K and V rings; as
+// deep as fits, two Q tiles preferred.
 bool plan_attn_pm_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnParams* a, size_t* bytes) {
   const bool fp8 = g->kv_dtype == TRTV_FP8_E4M3;
   const int nr = pl.rows_pad;
   const size_t qbuf = static_cast<size_t>(2) * nr * 128;
   const size_t qf8 = fp8 ? static_cast<size_t>(2) * 2 * nr * 128 : 0;
-  const size_t preg = 128 * 128;
+  const size_t preg = static_cast<size_t>(128 * 128) * nr / 16;  // four P^T buffers of 2 nr bytes per row
   const size_t kv = fp8 ? static_cast<size_t>(kGroups) * kBox : static_cast<size_t>(kGroups) * 2 * kBox;
   const int nitems = sparse ? pl.n_seq : g->batch;
   const size_t scan = align_up((static_cast<size_t>(nitems) + 1 + 32) * sizeof(int32_t), 16);
   const size_t ml = static_cast<size_t>(8 + 4 + 2) * nr * sizeof(float) + 8 * sizeof(int);  // + vote slots
-  const int np = 128 / (2 * nr);
   struct Depth { int nq, nk, nv; };
   static const Depth kBf16[] = {{2, 3, 3}, {1, 3, 3}, {2, 3, 2}, {2, 2, 2}};
-  static const Depth kFp8[] = {{2, 6, 6}, {2, 6, 5}, {2, 5, 5}, {2, 4, 4}, {2, 3, 3}, {2, 2, 2}};
+  static const Depth kFp8[] = {{2, 6, 6}, {2, 6, 5}, {2, 5, 5}, {2, 5, 4}, {2, 4, 4}, {2, 3, 3}, {2, 2, 2}};
   const Depth* list = fp8 ? kFp8 : kBf16;
-  const int nlist = fp8 ? 6 : 4;
+  const int nlist = fp8 ? 7 : 4;
   for (int i = 0; i < nlist; ++i) {
     const Depth d = list[i];
     size_t off = 0;
@@ -349,11 +349,11 @@ bool plan_attn_pm_smem(const trtv_geom* g, const Plan& pl, bool sparse, AttnPara
     a->off_ml = static_cast<int>(align_up(off, 16));
     off = a->off_ml + ml;
     a->off_bar = static_cast<int>(align_up(off, 8));
-    off = a->off_bar + (2 * d.nk + 2 * d.nv + 2 * np + 16) * sizeof(uint64_t) + 16;
+    off = a->off_bar + (2 * d.nk + 2 * d.nv + 24) * sizeof(uint64_t) + 16;
     a->nstages = d.nk;
     a->nv = d.nv;
     a->nq = d.nq;
-    a->np = np;
+    a->np = 4;
     a->qbuf = static_cast<int>(qbuf);
     a->off_k = a->off_v = a->off_conv = a->off_merge = 0;
     *bytes = off + kAlignSlack;

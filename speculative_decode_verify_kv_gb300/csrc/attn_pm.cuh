@@ -35,13 +35,17 @@
 //   O^T += V^T P^T  A = the V page read MN-major (head dims x positions), B =
 //                   P^T MN-major (rows x positions): 8 bf16 UMMA 128 x NR x 16
 //                   or 4 E4M3 UMMA 128 x 2NR x 32 -> TMEM O^T (lane = head dim)
-// After the softmax warps: one warp streams Q and the K pages, one issues the
-// UMMAs (one elected lane; QK of page i + 1 ahead of PV of page i), one streams
-// the V pages (rings of 32 KB bf16 or 16 KB E4M3 stages), and with FP8 caches
-// one turns each sequence's bf16 Q tile into the two E4M3 terms with a
-// power-of-two scale per row.  P^T lives in one 16 KB region of 128-byte rows: buffer b at byte
-// 2 NR b of each row (bf16: NR values; E4M3: NR hi bytes then NR lo bytes).
-// TMEM: two S^T buffers and O^T, each N columns wide.
+// Pages go through the QK, softmax and PV stages in pairs (of one sequence):
+// the softmax takes both pages of a pair in one pass -- one wait, one vote,
+// one barrier and one arrival per pair, and twice the independent arithmetic
+// between them.  After the softmax warps: one warp streams Q and the K pages,
+// one issues the UMMAs (one elected lane; QK of pair i + 1 ahead of PV of pair
+// i), one streams the V pages (rings of 32 KB bf16 or 16 KB E4M3 stages), and
+// with FP8 caches one turns each sequence's bf16 Q tile into the two E4M3
+// terms with a power-of-two scale per row.  P^T buffers live in 16 KB regions
+// of 128-byte rows, 2 NR bytes each (bf16: NR values; E4M3: NR hi bytes then
+// NR lo bytes).  TMEM: four S^T buffers (two pair slots) and O^T, each N
+// columns wide.
 #pragma once
 
 #include "attn.cuh"
@@ -116,10 +120,11 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
   constexpr int SW = FP8 ? 2 * NR : NR;  // UMMA N = TMEM columns of S^T and of O^T
   constexpr uint32_t IDESC_QK = FP8 ? umma_idesc_e4m3(128, SW) : umma_idesc_bf16(128, SW);
   constexpr uint32_t IDESC_PV = IDESC_QK | (1u << 15) | (1u << 16);  // A (V^T) and B (P^T) MN-major
-  constexpr uint32_t TM_O = 2 * SW;
-  constexpr uint32_t TMEM_COLS = 3 * SW <= 64 ? 64 : (3 * SW <= 128 ? 128 : 256);
-  constexpr int NP = 64 / NR;       // P^T buffers (2 NR bytes of each 128-byte row)
-  constexpr int LNP = NP == 2 ? 1 : 2;
+  // pages go through in pairs: S^T buffer / P^T buffer 2 s + e holds page e of
+  // the pair in slot s (two slots); O^T after the four S^T buffers
+  constexpr uint32_t TM_O = 4 * SW;
+  constexpr uint32_t TMEM_COLS = 5 * SW <= 128 ? 128 : (5 * SW <= 256 ? 256 : 512);
+  constexpr int BPR = 64 / NR;      // P^T buffers per 128-byte row (2 NR bytes each)
   static_assert(NR == 16 || NR == 32, "row tiles of 16 or 32");
 
   extern __shared__ uint8_t smem_raw[];
@@ -130,10 +135,10 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
   uint64_t* kempty = kfull + NK;   // QK finished reading the K stage
   uint64_t* vfull = kempty + NK;
   uint64_t* vempty = vfull + NV;   // PV finished reading the V stage
-  uint64_t* sfull = vempty + NV;   // [2] S^T written
-  uint64_t* pfull = sfull + 2;     // [NP] P^T written (8 softmax warps)
-  uint64_t* pvdone = pfull + NP;   // [NP] PV of the page in that P buffer retired
-  uint64_t* qfull = pvdone + NP;   // [2] bf16 Q tile landed
+  uint64_t* sfull = vempty + NV;   // [2 pair slots] S^T of the pair written
+  uint64_t* pfull = sfull + 2;     // [2] P^T of the pair written (the softmax warps)
+  uint64_t* pvdone = pfull + 2;    // [2] PV of the pair retired
+  uint64_t* qfull = pvdone + 2;    // [2] bf16 Q tile landed
   uint64_t* qempty = qfull + 2;    // [2] last QK of the sequence retired
   uint64_t* qcv = qempty + 2;      // [2] FP8: E4M3 Q terms and row scales written
   uint64_t* qsfree = qcv + 2;      // [2] FP8: the softmax warps have read the row scales
@@ -155,8 +160,11 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) { mbar_init(&kfull[i], 1); mbar_init(&kempty[i], 1); }
     for (int i = 0; i < NV; ++i) { mbar_init(&vfull[i], 1); mbar_init(&vempty[i], 1); }
-    for (int i = 0; i < 2; ++i) mbar_init(&sfull[i], 1);
-    for (int i = 0; i < NP; ++i) { mbar_init(&pfull[i], SMW); mbar_init(&pvdone[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&pfull[i], SMW);
+      mbar_init(&pvdone[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
@@ -308,45 +316,54 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
       return __all_sync(0xffffffffu, lane != 0 || mbar_wait(bar, par, wt));
     };
     bool alive = true;
-    int ks = 0, vs = 0, pb = 0;
-    uint32_t kph = 0, vph = 0, pph = 0, sb = 0;
-    auto issue_pv = [&](bool first) {
+    int ks = 0, vs = 0;
+    uint32_t kph = 0, vph = 0;
+    uint32_t qps = 0;             // pair slot of the next QK pair
+    uint32_t vps = 0, vpph = 0;   // pair slot of the next PV pair, and its pfull phase
+    // PV of a pair: n pages; `first`: the sequence's first pair (O^T starts over)
+    auto issue_pv = [&](int n, bool first) {
       if (!alive) return;
-      if (!wait1(&vfull[vs], vph) || !wait1(&pfull[pb], pph)) {
+      if (!wait1(&pfull[vps], vpph)) {
         alive = false;
         return;
       }
-      tc_fence_after();
-      const uint64_t va = desc_add(vd0, static_cast<uint32_t>(vs * KV));
-      const uint64_t pbd = desc_add(pd0, static_cast<uint32_t>(pb * 2 * NR));
-      if constexpr (FP8) {
-        // 32 positions per UMMA (32 V rows of 128 B = 4 KB); the 128 head
-        // dims are one swizzle atom; N = both P terms
+      for (int e = 0; e < n; ++e) {
+        if (!wait1(&vfull[vs], vph)) {
+          alive = false;
+          return;
+        }
+        tc_fence_after();
+        const uint64_t va = desc_add(vd0, static_cast<uint32_t>(vs * KV));
+        const int bi = 2 * vps + e;
+        const uint64_t pbd = desc_add(pd0, static_cast<uint32_t>((bi / BPR) * kPmPRegion + (bi % BPR) * 2 * NR));
+        const bool zero = first && e == 0;
+        if constexpr (FP8) {
+          // 32 positions per UMMA (32 V rows of 128 B = 4 KB); the 128 head
+          // dims are one swizzle atom; N = both P terms
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_e4m3_elect(tmem + TM_O, desc_add(va, kk * 4096), desc_add(pbd, kk * 4096), IDESC_PV,
-                          (!first || kk > 0) ? 1u : 0u);
-      } else {
-        // 16 positions per UMMA; the head dims' two 64-column atoms of the V
-        // stage are KV / 2 apart
+          for (int kk = 0; kk < 4; ++kk)
+            umma_e4m3_elect(tmem + TM_O, desc_add(va, kk * 4096), desc_add(pbd, kk * 4096), IDESC_PV,
+                            (!zero || kk > 0) ? 1u : 0u);
+        } else {
+          // 16 positions per UMMA; the head dims' two 64-column atoms of the V
+          // stage are KV / 2 apart
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_elect(tmem + TM_O, desc_add(va, kk * 2048), desc_add(pbd, kk * 2048), IDESC_PV,
-                          (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_elect(tmem + TM_O, desc_add(va, kk * 2048), desc_add(pbd, kk * 2048), IDESC_PV,
+                            (!zero || kk > 0) ? 1u : 0u);
+        }
+        umma_commit_elect(&vempty[vs]);
+        if (++vs == NV) {
+          vs = 0;
+          vph ^= 1u;
+        }
       }
-      umma_commit_elect(&vempty[vs]);
-      umma_commit_elect(&pvdone[pb]);
-      if (++vs == NV) {
-        vs = 0;
-        vph ^= 1u;
-      }
-      if (++pb == NP) {
-        pb = 0;
-        pph ^= 1u;
-      }
+      umma_commit_elect(&pvdone[vps]);
+      vps ^= 1u;
+      if (vps == 0) vpph ^= 1u;
     };
-    int sq = 0;
-    bool pend = false, pend_first = false;
+    int sq = 0, pend_n = 0;
+    bool pend_first = false;
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
          alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
          cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
@@ -357,43 +374,47 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
       }
       const uint64_t qd = desc_add(qd0, static_cast<uint32_t>(FP8 ? qs * 2 * NR * 128 : qb * QBUF));
       const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
-      for (int64_t j = j0; j < j1 && alive; ++j) {
-        // S buffer sb was last read by the softmax of the page two back, whose
-        // P this warp has already waited for (that page's PV went out first)
-        if (!wait1(&kfull[ks], kph)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t ka = desc_add(kd0, static_cast<uint32_t>(ks * KV));
-        const uint32_t sd = tmem + sb * SW;
-        if constexpr (FP8) {
-          // K = 32 head dims per UMMA; N = the hi and lo terms of the rows
+      for (int64_t j = j0; j < j1 && alive; j += 2) {
+        // S^T buffers of slot qps were last read by the softmax of the pair two
+        // back, whose P this warp has already waited for (that PV went first)
+        const int n = j + 1 < j1 ? 2 : 1;
+        for (int e = 0; e < n; ++e) {
+          if (!wait1(&kfull[ks], kph)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ka = desc_add(kd0, static_cast<uint32_t>(ks * KV));
+          const uint32_t sd = tmem + (2 * qps + e) * SW;
+          if constexpr (FP8) {
+            // K = 32 head dims per UMMA; N = the hi and lo terms of the rows
 #pragma unroll
-          for (int k = 0; k < D / 32; ++k)
-            umma_e4m3_elect(sd, desc_add(ka, k * 32), desc_add(qd, k * 32), IDESC_QK, k > 0);
-        } else {
+            for (int k = 0; k < D / 32; ++k)
+              umma_e4m3_elect(sd, desc_add(ka, k * 32), desc_add(qd, k * 32), IDESC_QK, k > 0);
+          } else {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            umma_bf16_elect(sd, desc_add(ka, (k >> 2) * (KV / 2) + (k & 3) * 32),
-                            desc_add(qd, (k >> 2) * qhalf + (k & 3) * 32), IDESC_QK, k > 0);
+            for (int k = 0; k < D / 16; ++k)
+              umma_bf16_elect(sd, desc_add(ka, (k >> 2) * (KV / 2) + (k & 3) * 32),
+                              desc_add(qd, (k >> 2) * qhalf + (k & 3) * 32), IDESC_QK, k > 0);
+          }
+          umma_commit_elect(&kempty[ks]);
+          if (++ks == NK) {
+            ks = 0;
+            kph ^= 1u;
+          }
         }
-        umma_commit_elect(&kempty[ks]);
-        umma_commit_elect(&sfull[sb]);
-        if (j == j1 - 1) umma_commit_elect(FP8 ? &qempty[qs] : &qempty[qb]);
-        if (++ks == NK) {
-          ks = 0;
-          kph ^= 1u;
-        }
-        sb ^= 1u;
-        if (pend) issue_pv(pend_first);
-        pend = true;
+        if (!alive) break;
+        umma_commit_elect(&sfull[qps]);
+        if (j + n == j1) umma_commit_elect(FP8 ? &qempty[qs] : &qempty[qb]);
+        qps ^= 1u;
+        if (pend_n > 0) issue_pv(pend_n, pend_first);
+        pend_n = n;
         pend_first = j == j0;
       }
       // the sequence's last PV goes out now: its epilogue must not wait for
       // the next sequence's Q tile and first QK
-      if (pend) issue_pv(pend_first);
-      pend = false;
+      if (pend_n > 0) issue_pv(pend_n, pend_first);
+      pend_n = 0;
     }
     umma_commit_elect(mdone);
     if (lane == 0) mbar_drain(mdone, 0, wt);
@@ -432,7 +453,7 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
     const int rows = G * T, lg = p.lg_group;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     bool dead = false;
-    int it = 0, sq = 0;
+    int it = 0, ip = 0, sq = 0;  // pages, pairs and sequences so far
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
          (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
          cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
@@ -457,59 +478,75 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
         mth[i] = -INFINITY;
         ls[i] = 0.f;
       }
-      for (int64_t j = j0; j < j1; ++j, ++it) {
-        const int sb = it & 1, pb = it & (NP - 1);
-        int blk = static_cast<int>(j);
-        uint32_t tokmask = 0xffffffffu;
-        if (sparse) {
-          blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
-          tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
-        }
-        if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[sb], static_cast<uint32_t>(it >> 1) & 1u, wt));
-        tc_fence_after();
-        uint32_t r[H];
-        tmem_ld_async(tl + sb * SW + col0, r);
-        if constexpr (FP8) {  // S = (Q_hi + Q_lo) K^T: add the lo half of N
-          uint32_t r2[H];
-          tmem_ld_async(tl + sb * SW + NR + col0, r2);
-          tmem_ld_wait_dep(r);
-          tmem_ld_wait_dep(r2);
+      for (int64_t j = j0; j < j1; j += 2, ++ip) {
+        const int n = j + 1 < j1 ? 2 : 1;     // pages of this pair
+        const int ps = ip & 1;                 // pair slot
+        const uint32_t pph = static_cast<uint32_t>(ip >> 1) & 1u;
+        int blk[2], pos0[2];
+        uint32_t tokmask[2] = {0xffffffffu, 0xffffffffu};
 #pragma unroll
-          for (int i = 0; i < H; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
-        } else {
-          tmem_ld_wait_dep(r);
+        for (int e = 0; e < 2; ++e) {
+          blk[e] = static_cast<int>(j) + e;
+          if (sparse && e < n) {
+            blk[e] = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j + e];
+            tokmask[e] = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j + e];
+          }
+          pos0[e] = blk[e] * kPage;
         }
-        const int pos0 = blk * kPage, pos = pos0 + kpos;
-        const bool masked = sparse || rows < NR || pos0 + kPage - 1 > L - T;
-        float x[H];
+        if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[ps], pph, wt));
+        tc_fence_after();
+        float x[2][H];
         bool over = false;  // a value above its column's reference maximum + 8
 #pragma unroll
-        for (int i = 0; i < H; ++i) {
-          float v = __uint_as_float(r[i]) * sc[i];
-          if (masked) {
-            const int c = col0 + i, t = c >> lg;
-            const bool ok = c < rows && pos <= L - T + t && ((tokmask >> t) & 1u);
-            v = ok ? v : -INFINITY;
+        for (int e = 0; e < 2; ++e) {
+          if (e >= n) {
+#pragma unroll
+            for (int i = 0; i < H; ++i) x[e][i] = -INFINITY;
+            continue;
           }
-          x[i] = v;
-          over |= v > mth[i];
+          const uint32_t sa = tl + (2 * ps + e) * SW + col0;
+          uint32_t r[H];
+          tmem_ld_async(sa, r);
+          if constexpr (FP8) {  // S = (Q_hi + Q_lo) K^T: add the lo half of N
+            uint32_t r2[H];
+            tmem_ld_async(sa + NR, r2);
+            tmem_ld_wait_dep(r);
+            tmem_ld_wait_dep(r2);
+#pragma unroll
+            for (int i = 0; i < H; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+          } else {
+            tmem_ld_wait_dep(r);
+          }
+          const int pos = pos0[e] + kpos;
+          const bool masked = sparse || rows < NR || pos0[e] + kPage - 1 > L - T;
+#pragma unroll
+          for (int i = 0; i < H; ++i) {
+            float v = __uint_as_float(r[i]) * sc[i];
+            if (masked) {
+              const int c = col0 + i, t = c >> lg;
+              const bool ok = c < rows && pos <= L - T + t && ((tokmask[e] >> t) & 1u);
+              v = ok ? v : -INFINITY;
+            }
+            x[e][i] = v;
+            over |= v > mth[i];
+          }
         }
-        // The reference maxima move only when some value of the page exceeds
-        // them by more than 8 (log2 domain): the warps of the column half vote,
-        // and only then are the exact column maxima exchanged (always on a
-        // sequence's first page, where the references are -inf).  The vote
-        // slot holds the page index of its last "yes", double-buffered by page
-        // parity; every warp of the half reads the same slot, so the barriers
+        // The reference maxima move only when some value of the pair exceeds
+        // them by more than 8 (log2 domain): the warps of the column group
+        // vote, and only then are the exact column maxima exchanged (always on
+        // a sequence's first pair, where the references are -inf).  The vote
+        // slot holds the pair index of its last "yes", double-buffered by pair
+        // parity; every warp of the group reads the same slot, so the barriers
         // below are taken alike.
-        volatile int* vote = pvote + (it & 1) * CG + cg;
-        if (__any_sync(0xffffffffu, over) && lane == 0) *vote = it;
+        volatile int* vote = pvote + (ip & 1) * CG + cg;
+        if (__any_sync(0xffffffffu, over) && lane == 0) *vote = ip;
         named_barrier(2 + cg, 128);
-        if (*vote == it) {
+        if (*vote == ip) {
           float red[H];
 #pragma unroll
-          for (int i = 0; i < H; ++i) red[i] = x[i];
+          for (int i = 0; i < H; ++i) red[i] = fmaxf(x[0][i], x[1][i]);
           const float cm = lane_col_reduce<H, true>(red, lane);
-          float* cb = cmax + (it & 1) * 4 * NR;
+          float* cb = cmax + (ip & 1) * 4 * NR;
           if ((lane & ((1 << (5 - LH)) - 1)) == 0) cb[q * NR + col0 + (lane >> (5 - LH))] = cm;
           named_barrier(2 + cg, 128);
           float mp[H];
@@ -525,7 +562,7 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
           }
           // first values of a column set its reference; a rise by more than 8
           // rescales the column's O^T and sum (the same decision in every
-          // thread of the half: it depends on shared values only)
+          // thread of the group: it depends on shared values only)
           bool need = false;
 #pragma unroll
           for (int i = 0; i < H; ++i) {
@@ -538,10 +575,11 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
             }
           }
           if (need) {
-            // O^T must be stable: PV of the previous page has retired
-            const int pv = it - 1;
+            // O^T must be stable: PV of the previous pair (of this sequence:
+            // a reference was set on an earlier pair) has retired
+            const int pv = ip - 1;
             if (!dead)
-              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[pv & (NP - 1)], static_cast<uint32_t>(pv >> LNP) & 1u, wt));
+              dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[pv & 1], static_cast<uint32_t>(pv >> 1) & 1u, wt));
             tc_fence_after();
             float alpha[H];
 #pragma unroll
@@ -562,75 +600,80 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
               tmem_ld_wait_dep(o);
 #pragma unroll
               for (int i = 0; i < H; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[i]);
-              if constexpr (H == 16) tmem_st16(tl + TM_O + half * NR + col0, o); else tmem_st8(tl + TM_O + half * NR + col0, o);
+              tmem_st8(tl + TM_O + half * NR + col0, o);
             }
             tmem_st_wait();
           }
         }
-        // P^T of this page into buffer pb, once PV of page it - NP has read it
-        if (it >= NP && !dead)
-          dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[pb], static_cast<uint32_t>((it >> LNP) - 1) & 1u, wt));
-        float pv[H];
+        // P^T of the pair into buffers 2 ps, 2 ps + 1, once PV of the pair two
+        // back (the same slot) has read them
+        if (ip >= 2 && !dead)
+          dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[ps], static_cast<uint32_t>((ip >> 1) - 1) & 1u, wt));
 #pragma unroll
-        for (int i = 0; i < H; ++i) {
-          pv[i] = m_use[i] == -INFINITY ? 0.f : fast_exp2(x[i] - m_use[i]);
-          ls[i] += pv[i];
-        }
-        const int pbyte = pb * 2 * NR;
-        if constexpr (FP8) {
-          uint32_t wh[H / 4], wl[H / 4];
+        for (int e = 0; e < 2; ++e) {
+          if (e >= n) continue;
+          float pv[H];
 #pragma unroll
-          for (int i = 0; i < H / 4; ++i) {
-            uint32_t h0, l0, h1, l1;
-            split_e4m3x2(__floats2half2_rn(pv[4 * i], pv[4 * i + 1]), h0, l0);
-            split_e4m3x2(__floats2half2_rn(pv[4 * i + 2], pv[4 * i + 3]), h1, l1);
-            wh[i] = (h0 & 0xFFFFu) | (h1 << 16);
-            wl[i] = (l0 & 0xFFFFu) | (l1 << 16);
+          for (int i = 0; i < H; ++i) {
+            pv[i] = m_use[i] == -INFINITY ? 0.f : fast_exp2(x[e][i] - m_use[i]);
+            ls[i] += pv[i];
           }
-          if constexpr (H == 16) {
-            st_sw128_u4(preg, kpos, pbyte + col0, wh[0], wh[1], wh[2], wh[3]);
-            st_sw128_u4(preg, kpos, pbyte + NR + col0, wl[0], wl[1], wl[2], wl[3]);
+          const int bi = 2 * ps + e;
+          uint8_t* pr = preg + (bi / BPR) * kPmPRegion;
+          const int pbyte = (bi % BPR) * 2 * NR;
+          if constexpr (FP8) {
+            uint32_t wh[H / 4], wl[H / 4];
+#pragma unroll
+            for (int i = 0; i < H / 4; ++i) {
+              uint32_t h0, l0, h1, l1;
+              split_e4m3x2(__floats2half2_rn(pv[4 * i], pv[4 * i + 1]), h0, l0);
+              split_e4m3x2(__floats2half2_rn(pv[4 * i + 2], pv[4 * i + 3]), h1, l1);
+              wh[i] = (h0 & 0xFFFFu) | (h1 << 16);
+              wl[i] = (l0 & 0xFFFFu) | (l1 << 16);
+            }
+            st_sw128_u2(pr, kpos, pbyte + col0, wh[0], wh[1]);
+            st_sw128_u2(pr, kpos, pbyte + NR + col0, wl[0], wl[1]);
           } else {
-            st_sw128_u2(preg, kpos, pbyte + col0, wh[0], wh[1]);
-            st_sw128_u2(preg, kpos, pbyte + NR + col0, wl[0], wl[1]);
-          }
-        } else {
-          uint32_t w[H / 2];
+            uint32_t w[H / 2];
 #pragma unroll
-          for (int i = 0; i < H / 2; ++i) {
-            __nv_bfloat162 pk = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
-            w[i] = *reinterpret_cast<uint32_t*>(&pk);
+            for (int i = 0; i < H / 2; ++i) {
+              __nv_bfloat162 pk = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
+              w[i] = *reinterpret_cast<uint32_t*>(&pk);
+            }
+            st_sw128_u4(pr, kpos, pbyte + 2 * col0, w[0], w[1], w[2], w[3]);
           }
-#pragma unroll
-          for (int i = 0; i < H / 8; ++i)
-            st_sw128_u4(preg, kpos, pbyte + 2 * col0 + 16 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
         fence_proxy_async_smem();
         // V rows at or past kv_len may hold anything (NaN included): P is zero
         // there, but 0 * NaN is not, so warp 0 zeroes them before PV reads V.
-        const int nvalid = L - pos0;
-        if (warp == 0 && nvalid < kPage) {
-          const int vs = it % NV;
-          if (!dead)
-            dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, wt));
-          uint8_t* vst = vring + vs * KV;
-          constexpr int NHALF = FP8 ? 1 : 2;  // 128-byte column blocks per token row
-          const int nchunks = (kPage - nvalid) * 8 * NHALF;
-          for (int idx = lane; idx < nchunks; idx += 32) {
-            const int tok = nvalid + idx / (8 * NHALF), part = idx % (8 * NHALF);
-            *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
-                                      (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+        if (warp == 0) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int nvalid = L - pos0[e];
+            if (e >= n || nvalid >= kPage) continue;
+            const int vs = (it + e) % NV;
+            if (!dead)
+              dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>((it + e) / NV) & 1u, wt));
+            uint8_t* vst = vring + vs * KV;
+            constexpr int NHALF = FP8 ? 1 : 2;  // 128-byte column blocks per token row
+            const int nchunks = (kPage - nvalid) * 8 * NHALF;
+            for (int idx = lane; idx < nchunks; idx += 32) {
+              const int tok = nvalid + idx / (8 * NHALF), part = idx % (8 * NHALF);
+              *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
+                                        (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
           }
           fence_proxy_async_smem();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pfull[pb]);
+        if (lane == 0) mbar_arrive(&pfull[ps]);
+        it += n;
       }
       // ------------------------------------------------------- sequence end
-      const int last = it - 1;
+      const int last = ip - 1;
       if (!dead)
-        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last & (NP - 1)], static_cast<uint32_t>(last >> LNP) & 1u, wt));
+        dead = __any_sync(0xffffffffu, !mbar_wait(&pvdone[last & 1], static_cast<uint32_t>(last >> 1) & 1u, wt));
       tc_fence_after();
       const float cs = lane_col_reduce<H, false>(ls, lane);
       if ((lane & ((1 << (5 - LH)) - 1)) == 0) lsm[q * NR + col0 + (lane >> (5 - LH))] = cs;

@@ -68,8 +68,8 @@ struct AttnParams {
   int off_q, off_vring, nv, nq;  // tcgen05 kernel: Q tiles (nq), V ring (nv); K ring at off_stage, nstages
   int qbuf;                      // tcgen05 kernel: bytes of one Q tile (rows x 256)
   int off_qf8;                   // tcgen05 kernel, FP8 caches: E4M3 Q tile (rows x 128 B)
-  // position-major tcgen05 kernel: P^T region (128 rows of 128 B holding np
-  // buffers of 2 * rows_pad bytes each) and log2 of the group
+  // position-major tcgen05 kernel: P^T regions (np buffers of 2 * rows_pad
+  // bytes in 128-byte rows) and log2 of the group
   int off_p, np, lg_group;
   int setup;                     // virtual units charged per sequence start (stream-K weight)
   // P32 sub-page tables (drafter attention): when set, group g of logical page
