@@ -337,20 +337,19 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
         const int bi = 2 * vps + e;
         const uint64_t pbd = desc_add(pd0, static_cast<uint32_t>((bi / BPR) * kPmPRegion + (bi % BPR) * 2 * NR));
         const bool zero = first && e == 0;
-        if constexpr (FP8) {
-          // 32 positions per UMMA (32 V rows of 128 B = 4 KB); the 128 head
-          // dims are one swizzle atom; N = both P terms
+        // FP8: 32 positions per UMMA (32 V rows of 128 B = 4 KB), the 128 head
+        // dims one swizzle atom, N = both P terms.  bf16: 16 positions per
+        // UMMA, the head dims' two 64-column atoms of the V stage KV / 2 apart.
+        constexpr uint32_t PSTEP = FP8 ? 4096 : 2048;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_e4m3_elect(tmem + TM_O, desc_add(va, kk * 4096), desc_add(pbd, kk * 4096), IDESC_PV,
-                            (!zero || kk > 0) ? 1u : 0u);
-        } else {
-          // 16 positions per UMMA; the head dims' two 64-column atoms of the V
-          // stage are KV / 2 apart
+        for (int h4 = 0; h4 < (FP8 ? 1 : 2); ++h4) {
+          uint64_t a[4], b[4];
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_elect(tmem + TM_O, desc_add(va, kk * 2048), desc_add(pbd, kk * 2048), IDESC_PV,
-                            (!zero || kk > 0) ? 1u : 0u);
+          for (int i = 0; i < 4; ++i) {
+            a[i] = desc_add(va, (4 * h4 + i) * PSTEP);
+            b[i] = desc_add(pbd, (4 * h4 + i) * PSTEP);
+          }
+          umma4_elect<FP8>(tmem + TM_O, a, b, IDESC_PV, (!zero || h4 > 0) ? 1u : 0u);
         }
         umma_commit_elect(&vempty[vs]);
         if (++vs == NV) {
@@ -386,16 +385,18 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
           tc_fence_after();
           const uint64_t ka = desc_add(kd0, static_cast<uint32_t>(ks * KV));
           const uint32_t sd = tmem + (2 * qps + e) * SW;
-          if constexpr (FP8) {
-            // K = 32 head dims per UMMA; N = the hi and lo terms of the rows
+          // FP8: K = 32 head dims per UMMA, N = the hi and lo terms of the rows;
+          // bf16: K = 16, the head dims' two 64-column halves KV / 2 (K page)
+          // and qhalf (Q tile) apart
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k)
-              umma_e4m3_elect(sd, desc_add(ka, k * 32), desc_add(qd, k * 32), IDESC_QK, k > 0);
-          } else {
+          for (int h4 = 0; h4 < (FP8 ? 1 : 2); ++h4) {
+            uint64_t a[4], b[4];
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-              umma_bf16_elect(sd, desc_add(ka, (k >> 2) * (KV / 2) + (k & 3) * 32),
-                              desc_add(qd, (k >> 2) * qhalf + (k & 3) * 32), IDESC_QK, k > 0);
+            for (int i = 0; i < 4; ++i) {
+              a[i] = desc_add(ka, FP8 ? i * 32 : h4 * (KV / 2) + i * 32);
+              b[i] = desc_add(qd, FP8 ? i * 32 : h4 * qhalf + i * 32);
+            }
+            umma4_elect<FP8>(sd, a, b, IDESC_QK, h4 > 0 ? 1u : 0u);
           }
           umma_commit_elect(&kempty[ks]);
           if (++ks == NK) {
@@ -471,10 +472,10 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&qsfree[qs]);
       }
-      float m_use[H], mth[H], ls[H];  // reference maxima, reference + 8, sums
+      // mth: the column's reference maximum + 8 (-inf until a first value)
+      float mth[H], ls[H];
 #pragma unroll
       for (int i = 0; i < H; ++i) {
-        m_use[i] = -INFINITY;
         mth[i] = -INFINITY;
         ls[i] = 0.f;
       }
@@ -566,13 +567,8 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
           bool need = false;
 #pragma unroll
           for (int i = 0; i < H; ++i) {
-            const float mn = fmaxf(m_use[i], mp[i]);
-            if (m_use[i] == -INFINITY) {
-              m_use[i] = mn;
-              mth[i] = mn + kRescaleLog2;
-            } else {
-              need |= mn > mth[i];
-            }
+            if (mth[i] == -INFINITY) mth[i] = mp[i] + kRescaleLog2;
+            else need |= mp[i] > mth[i];
           }
           if (need) {
             // O^T must be stable: PV of the previous pair (of this sequence:
@@ -584,14 +580,10 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
             float alpha[H];
 #pragma unroll
             for (int i = 0; i < H; ++i) {
-              const float mn = fmaxf(m_use[i], mp[i]);
-              const bool ni = mn > m_use[i] + kRescaleLog2;
-              alpha[i] = ni ? fast_exp2(m_use[i] - mn) : 1.f;
+              const bool ni = mp[i] > mth[i];
+              alpha[i] = ni ? fast_exp2(mth[i] - mp[i] - kRescaleLog2) : 1.f;
               ls[i] *= alpha[i];
-              if (ni) {
-                m_use[i] = mn;
-                mth[i] = mn + kRescaleLog2;
-              }
+              if (ni) mth[i] = mp[i] + kRescaleLog2;
             }
 #pragma unroll
             for (int half = 0; half < (FP8 ? 2 : 1); ++half) {  // FP8: the P_hi and P_lo parts of O^T
@@ -615,7 +607,7 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
           float pv[H];
 #pragma unroll
           for (int i = 0; i < H; ++i) {
-            pv[i] = m_use[i] == -INFINITY ? 0.f : fast_exp2(x[e][i] - m_use[i]);
+            pv[i] = mth[i] == -INFINITY ? 0.f : fast_exp2(x[e][i] - mth[i] + kRescaleLog2);
             ls[i] += pv[i];
           }
           const int bi = 2 * ps + e;
@@ -717,7 +709,8 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
           else static_cast<__nv_bfloat16*>(p.out)[orow] = __float2bfloat16(val * p.v_scale);
         } else {
           p.ws_o[(slot * p.rows_pad + c) * D + kpos] = val;
-          if (kpos == 0) p.ws_lse[slot * p.rows_pad + c] = lt[i] > 0.f ? m_use[i] + __log2f(lt[i]) : -INFINITY;
+          if (kpos == 0)
+            p.ws_lse[slot * p.rows_pad + c] = lt[i] > 0.f ? mth[i] - kRescaleLog2 + __log2f(lt[i]) : -INFINITY;
         }
       }
       tc_fence_before();
