@@ -186,6 +186,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended (not issuing) for up
+// to kSuspendNs while the phase is incomplete; it resumes when it completes.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded waits of one CTA.  A wait gives up after `limit_ns` (kWaitNs unless
 // a test shortens it): it sets TRTV_DEVERR_TIMEOUT and raises the CTA's abort
 // flag, after which every other wait of the CTA gives up at once, so each role
@@ -205,15 +220,15 @@ struct Waits {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waits& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*w.abort) return false;
-      if (global_timer_ns() - t0 > w.limit_ns) {
-        atomicOr(w.err, TRTV_DEVERR_TIMEOUT);
-        *w.abort = 1;
-        return false;
-      }
+  for (;;) {
+    // suspended in the wait rather than spinning: the warps that have work
+    // keep the issue slots
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (*w.abort) return false;
+    if (global_timer_ns() - t0 > w.limit_ns) {
+      atomicOr(w.err, TRTV_DEVERR_TIMEOUT);
+      *w.abort = 1;
+      return false;
     }
   }
 }
@@ -223,9 +238,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, const Waits& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitNs) {
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitNs) {
       atomicOr(w.err, TRTV_DEVERR_TIMEOUT);
       return false;
     }
