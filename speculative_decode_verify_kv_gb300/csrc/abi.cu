@@ -114,7 +114,7 @@ struct Plan {
   int group, group_pad, rows, mt, rows_pad, num_ctas, n_seq;
   int64_t pool_rows;
   // workspace
-  size_t ws_o, ws_lse, ws_splits, ws_blocks, ws_masks, ws_count, ws_sel, ws_total;
+  size_t ws_o, ws_lse, ws_splits, ws_blocks, ws_masks, ws_slots, ws_count, ws_sel, ws_total;
   int plan_cap;
 };
 
@@ -159,6 +159,8 @@ trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
   off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(int32_t), 256);
   p.ws_masks = off;
   off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(uint32_t), 256);
+  p.ws_slots = off;
+  off = align_up(off + static_cast<size_t>(p.n_seq) * p.plan_cap * sizeof(int32_t), 256);
   p.ws_count = off;
   off = align_up(off + (topk > 0 ? static_cast<size_t>(p.n_seq) * sizeof(int32_t) : 0), 256);
   p.ws_sel = off;  // fused proxy + top-k: pages done per sequence
@@ -490,6 +492,7 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   a.plan_blocks = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_blocks) : nullptr;
   a.plan_masks = sparse ? reinterpret_cast<const uint32_t*>(wsb + pl.ws_masks) : nullptr;
   a.plan_count = sparse ? reinterpret_cast<const int32_t*>(wsb + pl.ws_count) : nullptr;
+  a.plan_slots = sparse && !p32 ? reinterpret_cast<const int32_t*>(wsb + pl.ws_slots) : nullptr;
   a.err = err;
   a.batch = g->batch;
   a.qo_len = g->qo_len;
@@ -527,7 +530,8 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
                            g->max_pages_per_req, topk, pl.plan_cap,
                            reinterpret_cast<int32_t*>(wsb + pl.ws_blocks),
                            reinterpret_cast<uint32_t*>(wsb + pl.ws_masks),
-                           reinterpret_cast<int32_t*>(wsb + pl.ws_count), err, st);
+                           reinterpret_cast<int32_t*>(wsb + pl.ws_count), a.page_table, g->num_slots,
+                           const_cast<int32_t*>(a.plan_slots), err, st);
     if (e != cudaSuccess) return TRTV_ERR_CUDA;
   }
   e = pm     ? launch_attn_pm(g->kv_dtype == TRTV_FP8_E4M3, pl.rows_pad, map, qmap, a, pl.num_ctas, smem, st)

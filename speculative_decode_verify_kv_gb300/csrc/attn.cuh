@@ -208,6 +208,187 @@ __device__ __forceinline__ void write_split_desc(const AttnParams& p, const int3
   p.splits[k] = d;
 }
 
+// Sub-page buffer indices (units of one [Hk, 32, D] sub-page of the pool) of
+// the four 32-token groups of K or V page j of sequence `cur`, in two steps so
+// that no arithmetic waits on a load where the loads are issued:
+// page_lookup loads the page's slot (from the plan's slots -- sparse with a
+// page table -- or the page table) into sp[0], or with P32 tables resolves the
+// four sub-page indices (which needs kv_len L); page_buffers turns a looked-up
+// slot into the sub-page indices.  A bad slot sets TRTV_DEVERR_PAGE_ID (the
+// plan kernel has checked the plan's slots) when `flag` (one producer flags
+// it) and reads slot 0.
+__device__ __forceinline__ void page_lookup(const AttnParams& p, const SeqCursor& cur, int64_t j, bool sparse,
+                                            bool is_v, int L, int (&sp)[kGroups]) {
+  const int64_t e = static_cast<int64_t>(cur.s) * p.plan_cap + j;
+  if (sparse && p.plan_slots != nullptr) {
+    sp[0] = p.plan_slots[e];
+    return;
+  }
+  const int blk = sparse ? p.plan_blocks[e] : static_cast<int>(j);
+  const int64_t row = static_cast<int64_t>(cur.b) * p.max_pages + blk;
+  if (p.sub_k != nullptr) {
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g)
+      sp[g] = p32_entry(is_v ? p.sub_v : p.sub_k, row * kGroups + g, blk * kGroups + g, L, p.num_subpages, p.err);
+    return;
+  }
+  sp[0] = p.page_table[row];
+}
+
+__device__ __forceinline__ void page_buffers(const AttnParams& p, bool is_v, bool flag, int (&sp)[kGroups]) {
+  if (p.sub_k != nullptr) return;  // P32 tables: resolved by page_lookup
+  int slot = sp[0];
+  if (slot < 0 || slot >= p.num_slots) {
+    if (flag && p.plan_slots == nullptr) atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
+    slot = 0;
+  }
+  const int64_t buf = static_cast<int64_t>(slot) * p.slot_stride + (is_v ? 1 : 0);
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) sp[g] = static_cast<int>(buf * kGroups + g);
+}
+
+// Walk over the CTA's pages in order, across sequence ends: sequence `cur`,
+// page j of its real units [j0, j1) inside the CTA's range.
+struct PageWalk {
+  SeqCursor cur;
+  int64_t j, j0, j1;
+  bool valid;
+};
+
+__device__ __forceinline__ void walk_enter(PageWalk& w, int n, bool sparse, int64_t u0, int64_t u1, int setup) {
+  w.valid = (sparse ? w.cur.s : w.cur.b) < n && seq_in_range(w.cur, u1, setup);
+  w.j0 = w.j = w.valid ? seq_j0(w.cur, u0, setup) : 0;
+  w.j1 = w.valid ? seq_j1(w.cur, u1, setup) : 0;
+}
+
+__device__ __forceinline__ PageWalk walk_first(const int32_t* scan, int n, int Hk, bool sparse, int64_t u0,
+                                               int64_t u1, int setup) {
+  PageWalk w;
+  w.cur = cursor_first(scan, n, Hk, sparse, u0);
+  walk_enter(w, n, sparse, u0, u1, setup);
+  return w;
+}
+
+// advance k pages
+__device__ __forceinline__ void walk_skip(PageWalk& w, int64_t k, const int32_t* scan, int n, int Hk, bool sparse,
+                                          int64_t u0, int64_t u1, int setup) {
+  while (k > 0 && w.valid) {
+    const int64_t rem = w.j1 - w.j;
+    if (k < rem) {
+      w.j += k;
+      return;
+    }
+    k -= rem;
+    cursor_next(w.cur, scan, n, Hk, sparse);
+    walk_enter(w, n, sparse, u0, u1, setup);
+  }
+}
+
+// Page-ahead resolution for the pages of the CTA, 32 at a time (one page per
+// lane): `now` holds the current group of 32 pages, `next` the following one,
+// whose loads are in flight while `now` is used -- across sequence ends, so a
+// new sequence's first pages are never waited for.  (rs, rj) is the
+// (sequence, page) position of the group after `next` (rs = n past the range).
+struct PageAhead {
+  int now[kGroups], next[kGroups];
+  int rs, rj;
+};
+
+// Walk positioned at (rs, rj).
+__device__ __forceinline__ PageWalk walk_at(int rs, int rj, const int32_t* scan, int n, int Hk, bool sparse,
+                                            int64_t u0, int64_t u1, int setup) {
+  PageWalk x;
+  x.cur.s = rs;
+  x.cur.b = rs / Hk;
+  x.cur.h = rs % Hk;
+  if (rs < n * (sparse ? 1 : Hk)) cursor_fill(x.cur, scan, Hk, sparse);
+  walk_enter(x, n, sparse, u0, u1, setup);
+  if (x.valid) x.j = rj;
+  return x;
+}
+
+// Looks up this lane's page of the group at (rs, rj) (page_lookup); moves
+// (rs, rj) on by 32 pages.
+__device__ __forceinline__ void ahead_group(const AttnParams& p, int& rs, int& rj, int lane, bool sparse,
+                                            bool is_v, const int32_t* scan, int n, int Hk, int64_t u0, int64_t u1,
+                                            int (&sp)[kGroups]) {
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) sp[g] = 0;
+  const int end = n * (sparse ? 1 : Hk);
+  PageWalk x = walk_at(rs, rj, scan, n, Hk, sparse, u0, u1, p.setup);
+  PageWalk y = x;
+  walk_skip(y, lane, scan, n, Hk, sparse, u0, u1, p.setup);
+  if (y.valid) {
+    const int L = p.sub_k != nullptr ? p.kv_lens[y.cur.b] : 0;  // P32 tables: used entries
+    page_lookup(p, y.cur, y.j, sparse, is_v, L, sp);
+  }
+  walk_skip(x, 32, scan, n, Hk, sparse, u0, u1, p.setup);
+  rs = x.valid ? x.cur.s : end;
+  rj = x.valid ? static_cast<int>(x.j) : 0;
+}
+
+__device__ __forceinline__ void ahead_init(PageAhead& a, const AttnParams& p, const PageWalk& w, int lane,
+                                           bool sparse, bool is_v, const int32_t* scan, int n, int Hk, int64_t u0,
+                                           int64_t u1) {
+  a.rs = w.valid ? w.cur.s : n * (sparse ? 1 : Hk);
+  a.rj = w.valid ? static_cast<int>(w.j) : 0;
+  ahead_group(p, a.rs, a.rj, lane, sparse, is_v, scan, n, Hk, u0, u1, a.now);
+  ahead_group(p, a.rs, a.rj, lane, sparse, is_v, scan, n, Hk, u0, u1, a.next);
+}
+
+// after the 32 pages of `now` are used
+__device__ __forceinline__ void ahead_step(PageAhead& a, const AttnParams& p, int lane, bool sparse, bool is_v,
+                                           const int32_t* scan, int n, int Hk, int64_t u0, int64_t u1) {
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) a.now[g] = a.next[g];
+  ahead_group(p, a.rs, a.rj, lane, sparse, is_v, scan, n, Hk, u0, u1, a.next);
+}
+
+// The sparse plan entries (block, token mask) of the CTA's pages for the
+// softmax warps, 32 pages per group one group ahead, as PageAhead does the
+// buffers for the producers.  The walk position of the group after `next` is
+// kept as (sequence, page) only: the softmax holds few registers to spare.
+struct PlanAhead {
+  int blk_now, blk_next;
+  uint32_t m_now, m_next;
+  int rs, rj;
+};
+
+// Entries of group position (rs, rj) for this lane; returns the position 32
+// pages on (rs = n once past the CTA's range).
+__device__ __forceinline__ void plan_group(const AttnParams& p, int& rs, int& rj, int lane, const int32_t* scan,
+                                           int n, int Hk, int64_t u0, int64_t u1, int& blk, uint32_t& m) {
+  blk = 0;
+  m = 0;
+  PageWalk x = walk_at(rs, rj, scan, n, Hk, true, u0, u1, p.setup);
+  PageWalk y = x;
+  walk_skip(y, lane, scan, n, Hk, true, u0, u1, p.setup);
+  if (y.valid) {
+    const int64_t e = static_cast<int64_t>(y.cur.s) * p.plan_cap + y.j;
+    blk = p.plan_blocks[e];
+    m = p.plan_masks[e];
+  }
+  walk_skip(x, 32, scan, n, Hk, true, u0, u1, p.setup);
+  rs = x.valid ? x.cur.s : n;
+  rj = x.valid ? static_cast<int>(x.j) : 0;
+}
+
+__device__ __forceinline__ void plan_ahead_init(PlanAhead& a, const AttnParams& p, int lane, const int32_t* scan,
+                                                int n, int Hk, int64_t u0, int64_t u1) {
+  const PageWalk w = walk_first(scan, n, Hk, true, u0, u1, p.setup);
+  a.rs = w.valid ? w.cur.s : n;
+  a.rj = w.valid ? static_cast<int>(w.j) : 0;
+  plan_group(p, a.rs, a.rj, lane, scan, n, Hk, u0, u1, a.blk_now, a.m_now);
+  plan_group(p, a.rs, a.rj, lane, scan, n, Hk, u0, u1, a.blk_next, a.m_next);
+}
+
+__device__ __forceinline__ void plan_ahead_step(PlanAhead& a, const AttnParams& p, int lane, const int32_t* scan,
+                                                int n, int Hk, int64_t u0, int64_t u1) {
+  a.blk_now = a.blk_next;
+  a.m_now = a.m_next;
+  plan_group(p, a.rs, a.rj, lane, scan, n, Hk, u0, u1, a.blk_next, a.m_next);
+}
+
 template <bool FP8, int D, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ AttnParams p) {

@@ -113,9 +113,14 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   // one page of K (or V) for one head: 32 KB of bf16, or 16 KB of E4M3 used as
   // it is by kind::f8f6f4 UMMAs (Q and P then also E4M3)
   constexpr int KV = FP8 ? kGroups * kBox : kGroups * 2 * kBox;
-  constexpr uint32_t IDESC_QK = FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(128, 128);
-  constexpr uint32_t IDESC_PV = (FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(128, 128)) |
-                                (1u << 16);  // B (V) MN-major
+  // bf16 tiles of at most 64 rows use M = 64 UMMAs, whose accumulator (and
+  // TMEM A operand) row m sits in lane 32 (m / 16) + m % 16: 16 rows in every
+  // lane quadrant, so the softmax runs on all four SM sub-partitions (a warp
+  // reaches only its own quadrant's lanes) at the cost of an M = 128 UMMA.
+  const bool spread = !FP8 && p.rows_pad == 64;
+  const uint32_t IDESC_QK = FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(spread ? 64 : 128, 128);
+  const uint32_t IDESC_PV = (FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(spread ? 64 : 128, 128)) |
+                            (1u << 16);  // B (V) MN-major
   constexpr uint32_t TM_O = 384;
 
   extern __shared__ uint8_t smem_raw[];
@@ -197,6 +202,22 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   const int64_t u1 = cta_unit_begin(blockIdx.x + 1, W, p.num_ctas);
   if (u0 >= u1) return;
 
+  // The small loads the first pages need go out now, ahead of the TMEM
+  // allocation, the barrier below and the first wave of page copies: the
+  // producers' page buffers of the first 64 pages, and the softmax warps'
+  // plan entries and the first sequence's kv_len.
+  const bool producer = warp == 8 || warp == 10;
+  PageWalk pw{};
+  PageAhead pa{};
+  PlanAhead qa{};
+  int Lc = 0;  // softmax warps: kv_len of the sequence about to start
+  if (producer) {
+    pw = walk_first(scan, nitems, Hk, sparse, u0, u1, p.setup);
+    ahead_init(pa, p, pw, lane, sparse, warp == 10, scan, nitems, Hk, u0, u1);
+  } else if (warp < 8) {
+    if (sparse) plan_ahead_init(qa, p, lane, scan, nitems, Hk, u0, u1);
+    Lc = p.kv_lens[cursor_first(scan, nitems, Hk, sparse, u0).b];
+  }
   if (warp == 9) {
     tmem_alloc(tslot, kAttnTmemCols);
     tmem_relinquish();
@@ -211,175 +232,192 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   uint8_t* qf8 = smem + p.off_qf8;   // FP8: E4M3 Q tile, [rows][128 B], 128-byte swizzled
   float* qscale = reinterpret_cast<float*>(smem + p.off_ml);  // FP8: [128] per-row Q scales
 
-  if (warp == 8 || warp == 10) {
+  if (producer) {
     // ------------------------------------------- TMA producers: K (+Q) and V
     // Two independent streams: K pages are freed early (after QK), V pages
-    // late (after PV); one stream must not hold the other back.
+    // late (after PV); one stream must not hold the other back.  The pages'
+    // buffers come from the page-ahead groups (one page per lane, resolved 32
+    // to 64 pages early); lane 0 waits and issues.
+    const bool is_v = warp == 10;
     if (lane == 0) {
-      const bool is_v = warp == 10;
       prefetch_tensormap(&kv_map);
       if (!is_v) prefetch_tensormap(&q_map);
-      const uint64_t pol = policy_evict_first();
-      const int sub_rows = Hk * kSub;
-      const uint32_t qbytes = static_cast<uint32_t>(2 * 64 * 2 * G * T);
-      const int n = is_v ? NV : NK;
-      uint64_t* fullb = is_v ? vfull : kfull;
-      uint64_t* emptyb = is_v ? vempty : kempty;
-      uint8_t* ring = is_v ? vring : kring;
-      int it = 0, sq = 0;
-      bool alive = true;
-      for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-           alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
-           cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
-        if (!is_v) {
-          const int qb = sq % NQ;
-          if (sq >= NQ && !mbar_wait(&qempty[qb], static_cast<uint32_t>(sq / NQ - 1) & 1u, wt)) {
-            alive = false;
-            break;
-          }
+    }
+    const uint64_t pol = policy_evict_first();
+    const int sub_rows = Hk * kSub;
+    const uint32_t qbytes = static_cast<uint32_t>(2 * 64 * 2 * G * T);
+    const int n = is_v ? NV : NK;
+    uint64_t* fullb = is_v ? vfull : kfull;
+    uint64_t* emptyb = is_v ? vempty : kempty;
+    uint8_t* ring = is_v ? vring : kring;
+    int it = 0, sq = 0, st = 0;
+    uint32_t eph = 1;  // parity of the empty-barrier phase that frees stage st
+    PageWalk w = pw;
+    while (w.valid) {
+      if (!is_v && w.j == w.j0) {  // a sequence starts: its Q tile first
+        const int qb = sq % NQ;
+        bool ok = true;
+        if (lane == 0 && sq >= NQ) ok = mbar_wait(&qempty[qb], static_cast<uint32_t>(sq / NQ - 1) & 1u, wt);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (lane == 0) {
           mbar_arrive_expect_tx(&qfull[qb], qbytes);
           for (int hb = 0; hb < 2; ++hb)
             asm volatile(
                 "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                 " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(qbase + qb * QBUF + hb * (QBUF / 2))),
-                "l"(reinterpret_cast<uint64_t>(&q_map)), "r"(hb * 64), "r"(cur.h * G), "r"(cur.b * T),
+                "l"(reinterpret_cast<uint64_t>(&q_map)), "r"(hb * 64), "r"(w.cur.h * G), "r"(w.cur.b * T),
                 "r"(smem_u32(&qfull[qb]))
                 : "memory");
         }
-        const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
-        const int L = p.sub_k != nullptr ? p.kv_lens[cur.b] : 0;  // P32 tables: used entries
-        for (int64_t j = j0; j < j1; ++j, ++it) {
-          if (!is_v && p.withhold >= 0 && it >= p.withhold) {  // tests of the give-up path only
-            alive = false;
-            break;
-          }
-          const int blk = sparse ? p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j]
-                                 : static_cast<int>(j);
-          const int64_t row = static_cast<int64_t>(cur.b) * p.max_pages + blk;
-          int slot = 0;
-          if (p.sub_k == nullptr) {
-            slot = p.page_table[row];
-            if (slot < 0 || slot >= p.num_slots) {
-              if (!is_v) atomicOr(p.err, TRTV_DEVERR_PAGE_ID);
-              slot = 0;
-            }
-          }
-          const int64_t buf = static_cast<int64_t>(slot) * p.slot_stride + (is_v ? 1 : 0);
-          const int st = it % n;
-          if (it >= n && !mbar_wait(&emptyb[st], static_cast<uint32_t>(it / n - 1) & 1u, wt)) {
-            alive = false;
-            break;
-          }
-          uint8_t* dst = ring + st * KV;
-          mbar_arrive_expect_tx(&fullb[st], KV);
-          // bf16: two 128-byte column halves per sub-page; FP8: one box holds
-          // all 128 head dims of a token row
-#pragma unroll
-          for (int hb = 0; hb < (FP8 ? 1 : 2); ++hb)
-#pragma unroll
-            for (int g = 0; g < kGroups; ++g) {
-              const int sp = p.sub_k != nullptr
-                                 ? p32_entry(is_v ? p.sub_v : p.sub_k, row * kGroups + g,
-                                             blk * kGroups + g, L, p.num_subpages, p.err)
-                                 : static_cast<int>(buf * kGroups + g);
-              tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, &fullb[st], hb * 64,
-                          sp * sub_rows + cur.h * kSub, pol);
-            }
-        }
+        ++sq;
       }
-      // never leave copies in flight
+      if (!is_v && p.withhold >= 0 && it >= p.withhold) break;  // tests of the give-up path only
+      int spe[kGroups];
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) spe[g] = __shfl_sync(0xffffffffu, pa.now[g], it & 31);
+      page_buffers(p, is_v, !is_v, spe);
+      bool ok = true;
+      if (lane == 0 && it >= n) ok = mbar_wait(&emptyb[st], eph, wt);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) {
+        uint8_t* dst = ring + st * KV;
+        mbar_arrive_expect_tx(&fullb[st], KV);
+        // bf16: two 128-byte column halves per sub-page; FP8: one box holds
+        // all 128 head dims of a token row
+#pragma unroll
+        for (int hb = 0; hb < (FP8 ? 1 : 2); ++hb)
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g)
+            tma_load_2d(dst + (hb * kGroups + g) * kBox, &kv_map, &fullb[st], hb * 64,
+                        spe[g] * sub_rows + w.cur.h * kSub, pol);
+      }
+      if (++st == n) {
+        st = 0;
+        eph ^= 1u;
+      }
+      ++it;
+      walk_skip(w, 1, scan, nitems, Hk, sparse, u0, u1, p.setup);
+      if ((it & 31) == 0) ahead_step(pa, p, lane, sparse, is_v, scan, nitems, Hk, u0, u1);
+    }
+    // never leave copies in flight
+    if (lane == 0) {
       for (int k = (it > n ? it - n : 0); k < it; ++k)
         mbar_drain(&fullb[k % n], static_cast<uint32_t>(k / n) & 1u, wt);
       if (!is_v && sq >= 1)
         mbar_drain(&qfull[(sq - 1) % NQ], static_cast<uint32_t>((sq - 1) / NQ) & 1u, wt);
     }
+    __syncwarp();
   } else if (warp == 9) {
     // ----------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
-      bool alive = true;
-      auto issue_pv = [&](int pg, bool first) {
-        const int vs = pg % NV, b = pg % kSBufs;
-        if (!alive) return;
-        if (!mbar_wait(&vfull[vs], static_cast<uint32_t>(pg / NV) & 1u, wt) ||
-            !mbar_wait(&pfull[b], static_cast<uint32_t>(pg / kSBufs) & 1u, wt)) {
-          alive = false;
-          return;
+    // The whole warp runs the loop (uniform control flow, operands in uniform
+    // registers) and one elected lane issues; lane 0 waits for the barriers.
+    // Descriptors are built once and moved by byte offsets; ring positions
+    // advance by increments (no division in the loop).
+    const uint64_t kd0 = umma_desc_sw128(smem_u32(kring));
+    const uint64_t qd0 = umma_desc_sw128(smem_u32(FP8 ? qf8 : qbase));
+    const uint64_t vd0 = FP8 ? umma_desc_sw128_lbo_sbo(smem_u32(vring), 1024, 1024)
+                             : umma_desc_sw128_mn(smem_u32(vring), KV / 2);
+    auto wait1 = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, lane != 0 || mbar_wait(bar, par, wt));
+    };
+    bool alive = true;
+    int ks = 0, vs = 0, sb = 0, pb = 0, qb = 0;
+    uint32_t kph = 0, vph = 0, sph = 0, pph = 0, qph = 0;
+    int it = 0;
+    // O += P V for the next page in PV order (S buffer pb, V stage vs);
+    // `first`: the sequence's first page (O starts over)
+    auto issue_pv = [&](bool first) {
+      if (!alive) return;
+      if (!wait1(&vfull[vs], vph) || !wait1(&pfull[pb], pph)) {
+        alive = false;
+        return;
+      }
+      tc_fence_after();
+      const uint64_t va = desc_add(vd0, static_cast<uint32_t>(vs * KV));
+      const uint32_t pa = tmem + static_cast<uint32_t>(pb * 128);
+      // FP8: 32 tokens (8 P columns, 32 V rows of 128 B = 4 KB) per UMMA, all
+      // 128 head dims one swizzle atom, O += P_hi V + P_lo V (P_hi in columns
+      // 0..31, P_lo in 32..63).  bf16: 16 tokens per UMMA, both 64-column
+      // halves of V in one instruction.
+#pragma unroll
+      for (int h4 = 0; h4 < 2; ++h4) {
+        uint32_t a[4];
+        uint64_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          a[i] = FP8 ? pa + h4 * 32 + i * 8 : pa + (4 * h4 + i) * 8;
+          b[i] = desc_add(va, FP8 ? i * 4096 : (4 * h4 + i) * 2048);
         }
-        tc_fence_after();
-        const uint32_t v0 = smem_u32(vring + vs * KV);
-        if constexpr (FP8) {
-          // E4M3: 32 tokens (8 P columns, 32 V rows of 128 B = 4 KB) per UMMA;
-          // all 128 head dims are one 128-byte swizzle atom
-          // O += P_hi V + P_lo V (P_hi in columns 0..31, P_lo in 32..63)
-#pragma unroll
-          for (int term = 0; term < 2; ++term)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_e4m3_tmem_a(tmem + TM_O, tmem + b * 128 + term * 32 + kk * 8,
-                               umma_desc_sw128_lbo_sbo(v0 + kk * 4096, 1024, 1024), IDESC_PV,
-                               (!first || (term | kk) > 0) ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_tmem_a(tmem + TM_O, tmem + b * 128 + kk * 8, umma_desc_sw128_mn(v0 + kk * 2048, KV / 2),
-                             IDESC_PV, (!first || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&vempty[vs]);
-        umma_commit(&pvdone[b]);
-      };
-      int it = 0, sq = 0, pend = -1;
-      bool pend_first = false;
-      for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
-           alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
-           cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
-        const int qb = sq % NQ;
-        if (!mbar_wait(FP8 ? &qcv[qb] : &qfull[qb], static_cast<uint32_t>(sq / NQ) & 1u, wt)) {
+        umma4_tmem_a_elect<FP8>(tmem + TM_O, a, b, IDESC_PV, (!first || h4 > 0) ? 1u : 0u);
+      }
+      umma_commit_elect(&vempty[vs]);
+      umma_commit_elect(&pvdone[pb]);
+      if (++vs == NV) {
+        vs = 0;
+        vph ^= 1u;
+      }
+      if (++pb == kSBufs) {
+        pb = 0;
+        pph ^= 1u;
+      }
+    };
+    bool pend = false, pend_first = false;
+    for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+         alive && (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
+         cursor_next(cur, scan, nitems, Hk, sparse)) {
+      if (!wait1(FP8 ? &qcv[qb] : &qfull[qb], qph)) {
+        alive = false;
+        break;
+      }
+      const uint64_t qd = desc_add(qd0, static_cast<uint32_t>(FP8 ? 0 : qb * QBUF));
+      const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
+      for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
+        // S buffer sb was last read by the PV of page it - 3
+        if (!wait1(&kfull[ks], kph) || (it >= kSBufs && !wait1(&pvdone[sb], sph ^ 1u))) {
           alive = false;
           break;
         }
-        const uint32_t a0 = smem_u32(qbase + qb * QBUF);
-        const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
-        for (int64_t j = j0; j < j1 && alive; ++j, ++it) {
-          const int ks = it % NK, buf = it % kSBufs;
-          if (!mbar_wait(&kfull[ks], static_cast<uint32_t>(it / NK) & 1u, wt) ||
-              (it >= kSBufs && !mbar_wait(&pvdone[buf], static_cast<uint32_t>(it / kSBufs - 1) & 1u, wt))) {
-            alive = false;
-            break;
+        tc_fence_after();
+        const uint64_t ka = desc_add(kd0, static_cast<uint32_t>(ks * KV));
+        // FP8: a 128-byte row holds all 128 head dims, K = 32 per UMMA,
+        // S = Q_hi K^T + Q_lo K^T.  bf16: K = 16, the head dims' two 64-column
+        // halves KV / 2 (K page) and QBUF / 2 (Q tile) apart.
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4) {
+          uint64_t a[4], b[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            a[i] = desc_add(qd, FP8 ? h4 * kQf8Tile + i * 32 : h4 * (QBUF / 2) + i * 32);
+            b[i] = desc_add(ka, FP8 ? i * 32 : h4 * (KV / 2) + i * 32);
           }
-          tc_fence_after();
-          const uint32_t k0 = smem_u32(kring + ks * KV);
-          if constexpr (FP8) {
-            // E4M3: a 128-byte row holds all 128 head dims; K = 32 per UMMA;
-            // S = Q_hi K^T + Q_lo K^T
-#pragma unroll
-            for (int term = 0; term < 2; ++term) {
-              const uint32_t q0 = smem_u32(qf8 + term * kQf8Tile);
-#pragma unroll
-              for (int k = 0; k < D / 32; ++k)
-                umma_e4m3(tmem + buf * 128, umma_desc_sw128(q0 + k * 32), umma_desc_sw128(k0 + k * 32), IDESC_QK,
-                          (term | k) > 0);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-              umma_bf16(tmem + buf * 128, umma_desc_sw128(a0 + (k >> 2) * (QBUF / 2) + (k & 3) * 32),
-                        umma_desc_sw128(k0 + (k >> 2) * (KV / 2) + (k & 3) * 32), IDESC_QK, k > 0);
-          }
-          umma_commit(&kempty[ks]);
-          umma_commit(&sfull[buf]);
-          if (j == j1 - 1) umma_commit(&qempty[qb]);
-          if (pend >= 0) issue_pv(pend, pend_first);
-          pend = it;
-          pend_first = j == j0;
+          umma4_elect<FP8>(tmem + static_cast<uint32_t>(sb * 128), a, b, IDESC_QK, h4 > 0 ? 1u : 0u);
         }
-        // the sequence's last PV goes out now: its epilogue must not wait for
-        // the next sequence's Q tile and first QK
-        if (pend >= 0) issue_pv(pend, pend_first);
-        pend = -1;
+        umma_commit_elect(&kempty[ks]);
+        umma_commit_elect(&sfull[sb]);
+        if (j == j1 - 1) umma_commit_elect(&qempty[qb]);
+        if (++ks == NK) {
+          ks = 0;
+          kph ^= 1u;
+        }
+        if (++sb == kSBufs) {
+          sb = 0;
+          sph ^= 1u;
+        }
+        if (pend) issue_pv(pend_first);
+        pend = true;
+        pend_first = j == j0;
       }
-      umma_commit(mdone);
-      mbar_drain(mdone, 0, wt);
+      // the sequence's last PV goes out now: its epilogue must not wait for
+      // the next sequence's Q tile and first QK
+      if (pend) issue_pv(pend_first);
+      pend = false;
+      if (++qb == NQ) {
+        qb = 0;
+        qph ^= 1u;
+      }
     }
+    umma_commit_elect(mdone);
+    if (lane == 0) mbar_drain(mdone, 0, wt);
     __syncwarp();
   } else {
     // -------------------------------------------------- softmax and epilogue
@@ -411,10 +449,11 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         if (lane == 0) mbar_arrive(&qcv[qb]);
       }
     } else {
-    const int r = 32 * q + lane;
-    const int t = r / G, gl = r % G;
+    const int r = 32 * q + lane;                                   // this thread's TMEM lane
+    const int row = spread ? (lane < 16 ? 16 * q + lane : 1 << 20) : r;  // its (token, group head) row
+    const int t = row / G, gl = row % G;
     const bool valid = t < T;
-    const bool live = 32 * q < G * T;  // same for both warps of a quadrant
+    const bool live = spread || 32 * q < G * T;  // same for both warps of a quadrant
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     float* xmax = ml + 512;            // [2 pages][2 halves][128 rows]
     float* xl = ml + 1024;             // [2 halves][128 rows]
@@ -423,7 +462,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
          (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
          cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
-      const int L = p.kv_lens[cur.b];
+      const int L = Lc;
+      {  // the next sequence's kv_len loads a whole sequence ahead of its use
+        SeqCursor nx = cur;
+        cursor_next(nx, scan, nitems, Hk, sparse);
+        if ((sparse ? nx.s : nx.b) < nitems) Lc = p.kv_lens[nx.b];
+      }
       const int bound = valid ? L - T + t : -1;
       const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
       float m_use = -INFINITY, l = 0.f;
@@ -438,13 +482,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
       }
       for (int64_t j = j0; j < j1; ++j, ++it) {
         const int buf = it % kSBufs;
-        // the page's plan entry is loaded before the wait, so its latency
-        // overlaps the QK rather than the softmax
         int blk = static_cast<int>(j);
         uint32_t tokmask = 0xffffffffu;
-        if (sparse) {
-          blk = p.plan_blocks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
-          tokmask = p.plan_masks[static_cast<int64_t>(cur.s) * p.plan_cap + j];
+        if (sparse) {  // the page's plan entry, loaded 32 to 64 pages ahead
+          if (it > 0 && (it & 31) == 0) plan_ahead_step(qa, p, lane, scan, nitems, Hk, u0, u1);
+          blk = __shfl_sync(0xffffffffu, qa.blk_now, it & 31);
+          tokmask = __shfl_sync(0xffffffffu, qa.m_now, it & 31);
         }
         if (!dead)
           dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, wt));
@@ -485,13 +528,13 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
               m_use = m_new;
             }
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-              uint32_t w[32];
-              tmem_ld32_async(tl + TM_O + hf * 64 + c0, w);
+            for (int c0 = 0; c0 < 64; c0 += 16) {  // 16 columns at a time: x[] stays live meanwhile
+              uint32_t w[16];
+              tmem_ld_async(tl + TM_O + hf * 64 + c0, w);
               tmem_ld_wait_dep(w);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-              tmem_st32(tl + TM_O + hf * 64 + c0, w);
+              for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+              tmem_st16(tl + TM_O + hf * 64 + c0, w);
             }
             tmem_st_wait();
           }
@@ -518,16 +561,20 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
             tmem_st16(tl + buf * 128 + hf * 16, wh);
             tmem_st16(tl + buf * 128 + 32 + hf * 16, wl);
           } else {
-            uint32_t w[32];
+            // two halves of 16 columns: fewer values live at once
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float p0 = none ? 0.f : fast_exp2(x[2 * i] - m_use);
-              const float p1 = none ? 0.f : fast_exp2(x[2 * i + 1] - m_use);
-              l += p0 + p1;
-              __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-              w[i] = *reinterpret_cast<uint32_t*>(&pk);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float p0 = none ? 0.f : fast_exp2(x[32 * h2 + 2 * i] - m_use);
+                const float p1 = none ? 0.f : fast_exp2(x[32 * h2 + 2 * i + 1] - m_use);
+                l += p0 + p1;
+                __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                w[i] = *reinterpret_cast<uint32_t*>(&pk);
+              }
+              tmem_st16(tl + buf * 128 + hf * 32 + 16 * h2, w);
             }
-            tmem_st32(tl + buf * 128 + hf * 32, w);
           }
           tmem_st_wait();
         }
@@ -598,14 +645,14 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
                 }
               }
             } else {
-              float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * p.rows_pad + r) * D + hf * 64 + c0);
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * p.rows_pad + row) * D + hf * 64 + c0);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(__uint_as_float(v[4 * i]) * sc, __uint_as_float(v[4 * i + 1]) * sc,
                                      __uint_as_float(v[4 * i + 2]) * sc, __uint_as_float(v[4 * i + 3]) * sc);
             }
           }
-          if (!whole && hf == 0) p.ws_lse[slot * p.rows_pad + r] = lt > 0.f ? m_use + __log2f(lt) : -INFINITY;
+          if (!whole && hf == 0) p.ws_lse[slot * p.rows_pad + row] = lt > 0.f ? m_use + __log2f(lt) : -INFINITY;
         }
       }
       tc_fence_before();

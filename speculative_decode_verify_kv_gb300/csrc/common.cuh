@@ -57,6 +57,9 @@ struct AttnParams {
   const int32_t* plan_blocks;   // sparse: [n_seq, plan_cap] selected blocks
   const uint32_t* plan_masks;   // sparse: [n_seq, plan_cap] token bitmasks
   const int32_t* plan_count;    // sparse: [n_seq]
+  // sparse with a page table: [n_seq, plan_cap] page-table slot of each
+  // selected block (checked by the plan kernel), so a page costs one load
+  const int32_t* plan_slots;
   int* err;
   int batch, qo_len, num_q_heads, num_kv_heads, group, group_pad, head_dim;
   int max_pages, num_slots, slot_stride, rows, rows_pad;
@@ -352,7 +355,11 @@ __device__ void block_exclusive_scan(int n, int32_t* scan, int32_t* warp_tot, F 
   const int seg = (n + nthr - 1) / nthr;
   const int lo = min(n, tid * seg), hi = min(n, lo + seg);
   int32_t local = 0;
-  for (int i = lo; i < hi; ++i) local += count(i);
+  for (int i = lo; i < hi; ++i) {  // each count is taken once (it may be a global load)
+    const int32_t c = count(i);
+    scan[i] = c;
+    local += c;
+  }
   int32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -373,8 +380,9 @@ __device__ void block_exclusive_scan(int n, int32_t* scan, int32_t* warp_tot, F 
   __syncthreads();
   int32_t run = warp_tot[warp] + incl - local;
   for (int i = lo; i < hi; ++i) {
+    const int32_t c = scan[i];
     scan[i] = run;
-    run += count(i);
+    run += c;
   }
   __syncthreads();
 }

@@ -45,7 +45,8 @@ cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t*
 cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
                                int num_kv_heads, int max_pages, int topk, int plan_cap,
                                int32_t* plan_blocks, uint32_t* plan_masks, int32_t* plan_count,
-                               int* err, cudaStream_t st);
+                               const int32_t* pt, int num_slots, int32_t* plan_slots, int* err,
+                               cudaStream_t st);
 cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int qo_len,
                         int num_kv_heads, int max_pages, int topk, int32_t* out, int* err,
                         cudaStream_t st);

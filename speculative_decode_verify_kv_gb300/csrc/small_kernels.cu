@@ -54,12 +54,15 @@ __global__ void subpage_view_kernel(const int32_t* __restrict__ pt, const int32_
 // (b, h): mask[v] = bitmask of tokens t whose list selected block v; a token
 // whose list holds an index >= max_pages selects nothing (its rows are zero)
 // and raises TRTV_DEVERR_BLOCK_IDX; blocks at or past kv_len are dropped
-// (no token sees them).  Output: ascending unique blocks with their masks.
+// (no token sees them).  Output: ascending unique blocks with their masks,
+// and (given the page table `pt`) each block's slot, a slot outside the pool
+// raising TRTV_DEVERR_PAGE_ID and reading as slot 0.
 __global__ void sparse_plan_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ lens,
                                    int batch, int qo_len, int num_kv_heads, int max_pages, int topk,
                                    int plan_cap, int32_t* __restrict__ plan_blocks,
                                    uint32_t* __restrict__ plan_masks, int32_t* __restrict__ plan_count,
-                                   int* err) {
+                                   const int32_t* __restrict__ pt, int num_slots,
+                                   int32_t* __restrict__ plan_slots, int* err) {
   extern __shared__ uint32_t mask[];  // [max_pages]
   __shared__ uint32_t bad_tokens;
   __shared__ int32_t warp_tot[32];
@@ -122,6 +125,14 @@ __global__ void sparse_plan_kernel(const int32_t* __restrict__ idx, const int32_
     if (m != 0) {
       plan_blocks[static_cast<int64_t>(s) * plan_cap + pos] = i;
       plan_masks[static_cast<int64_t>(s) * plan_cap + pos] = m;
+      if (pt != nullptr) {
+        int slot = pt[static_cast<int64_t>(b) * max_pages + i];
+        if (slot < 0 || slot >= num_slots) {
+          atomicOr(err, TRTV_DEVERR_PAGE_ID);
+          slot = 0;
+        }
+        plan_slots[static_cast<int64_t>(s) * plan_cap + pos] = slot;
+      }
       ++pos;
     }
   }
@@ -160,27 +171,29 @@ __global__ void topk_kernel(const float* __restrict__ scores, const int32_t* __r
 // lse_i equals softmax over the union: o = sum_i 2^(lse_i - M) o_i /
 // sum_i 2^(lse_i - M), M = max_i lse_i (the ladder and sparse passes of
 // "... verify" attend each row's visible positions exactly once, whichever
-// piece holds them).  One CTA per (CTA boundary k, chunk of 8 rows for
-// head_dim 128, 16 for 64; one float4 per thread): boundary k's
+// piece holds them).  One CTA per (CTA boundary k, chunk of 32 rows; four
+// float4 per thread for head_dim 128, two for 64): boundary k's
 // descriptor names the cut sequence it starts (or none); contributors are
-// summed in CTA order, so the result does not depend on timing.  Launched with
+// summed in CTA order, so the result does not depend on timing.  Each thread
+// holds several elements, so one wave of CTAs covers every cut sequence and
+// each thread keeps many independent loads in flight.  Launched with
 // programmatic dependent launch right after the attention kernel: the CTAs
 // wait (pdl_wait) until that kernel has finished and its partials are visible.
 constexpr int kCombineThreads = 256;
-// rows per CTA: one float4 of one row per thread
-__host__ __device__ constexpr int combine_rows(int D) { return kCombineThreads * 4 / D; }
+// rows per CTA
+__host__ __device__ constexpr int combine_rows(int) { return 32; }
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnParams p) {
   constexpr int F4 = D / 4;         // float4 per row
   constexpr int R = combine_rows(D);  // rows of this CTA's chunk
-  constexpr int EL = R * F4 / kCombineThreads;  // elements per thread (1)
+  constexpr int EL = R * F4 / kCombineThreads;  // elements per thread (4 or 2)
   constexpr int CU = 4;             // contributors per batch of loads
   __shared__ int4 desc[2];
   __shared__ int slots[kMaxCombineParts];
   pdl_wait();
   pdl_trigger();
-  const int nch = p.rows_pad / R;
+  const int nch = (p.rows_pad + R - 1) / R;
   const int k = 1 + blockIdx.x / nch, chunk = blockIdx.x % nch;
   const int tid = threadIdx.x;
   if (tid < 2) desc[tid] = __ldcg(reinterpret_cast<const int4*>(p.splits + k) + tid);
@@ -221,8 +234,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
       const int64_t sa = sl >= 0 ? sl : s0;
 #pragma unroll
       for (int u = 0; u < EL; ++u) {
-        x[u][j] = __ldcg(p.ws_lse + sa * rows + r[u]);
-        v[u][j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sa * rows + r[u]) * D + d[u]));
+        const int rr = r[u] < rows ? r[u] : 0;  // rows past the tile (a 16-row tile) read row 0, unused
+        x[u][j] = __ldcg(p.ws_lse + sa * rows + rr);
+        v[u][j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sa * rows + rr) * D + d[u]));
         if (sl < 0) x[u][j] = -INFINITY;
       }
     }
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 #pragma unroll
   for (int u = 0; u < EL; ++u) {
     const int t = r[u] / p.group_pad, gl = r[u] % p.group_pad;
-    if (t >= p.qo_len || gl >= p.group) continue;
+    if (r[u] >= rows || t >= p.qo_len || gl >= p.group) continue;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);  // no visible position in any piece
     if (l[u] > 0.f) {
       const float inv = p.v_scale / l[u];
@@ -435,7 +449,8 @@ cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t*
 cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
                                int num_kv_heads, int max_pages, int topk, int plan_cap,
                                int32_t* plan_blocks, uint32_t* plan_masks, int32_t* plan_count,
-                               int* err, cudaStream_t st) {
+                               const int32_t* pt, int num_slots, int32_t* plan_slots, int* err,
+                               cudaStream_t st) {
   const size_t smem = static_cast<size_t>(max_pages) * sizeof(uint32_t);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(sparse_plan_kernel,
@@ -445,7 +460,7 @@ cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batc
   }
   return launch_pdl(sparse_plan_kernel, dim3(batch * num_kv_heads), dim3(256), smem, st, idx, lens, batch,
                     qo_len, num_kv_heads, max_pages, topk, plan_cap, plan_blocks, plan_masks, plan_count,
-                    err);
+                    pt, num_slots, plan_slots, err);
 }
 
 cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int qo_len,
@@ -459,7 +474,8 @@ cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t st) {
   if (p.num_ctas < 2) return cudaSuccess;  // no CTA boundary, nothing is cut
-  const dim3 grid(static_cast<unsigned>((p.num_ctas - 1) * (p.rows_pad / combine_rows(head_dim))));
+  const int nch = (p.rows_pad + combine_rows(head_dim) - 1) / combine_rows(head_dim);
+  const dim3 grid(static_cast<unsigned>((p.num_ctas - 1) * nch));
   return head_dim == 64 ? launch_pdl(combine_kernel<64>, grid, dim3(kCombineThreads), 0, st, p)
                         : launch_pdl(combine_kernel<128>, grid, dim3(kCombineThreads), 0, st, p);
 }

@@ -329,3 +329,39 @@ __device__ __forceinline__ void umma4_elect(uint32_t d_tmem, const uint64_t (&a)
 }
 
 }  // namespace trtv
+
+namespace trtv {
+
+// Four UMMAs into one accumulator with A read from tensor memory (columns
+// a[i]) and B from shared memory (descriptors b[i]), issued by one elected
+// lane of the warp (the whole warp executes the call); the first accumulates
+// only if `acc_first`, the others always.
+template <bool FP8>
+__device__ __forceinline__ void umma4_tmem_a_elect(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                                   uint32_t idesc, uint32_t acc_first) {
+  if constexpr (FP8) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 t, 1, 1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %9, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %6, %9, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%7], %8, %9, t;\n\t}\n" ::"r"(d_tmem),
+        "r"(a[0]), "l"(b[0]), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]), "l"(b[3]), "r"(idesc),
+        "r"(acc_first)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 t, 1, 1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %9, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %9, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %9, t;\n\t}\n" ::"r"(d_tmem),
+        "r"(a[0]), "l"(b[0]), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]), "l"(b[3]), "r"(idesc),
+        "r"(acc_first)
+        : "memory");
+  }
+}
+
+}  // namespace trtv
