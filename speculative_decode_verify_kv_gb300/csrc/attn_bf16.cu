@@ -36,8 +36,14 @@ cudaError_t launch_attn_bf16(int head_dim, int mt, const CUtensorMap& map, const
 
 cudaError_t launch_attn_umma(const CUtensorMap& kv_map, const CUtensorMap& q_map, const AttnParams& p,
                              int grid, size_t smem, cudaStream_t st) {
-  const void* fn = reinterpret_cast<const void*>(&attn_umma_kernel<128, false>);
-  cudaError_t e = ensure_smem_attr(fn, smem);
+  // 64-row tiles: M = 64 UMMAs with 16 rows in every TMEM lane quadrant
+  if (p.rows_pad == 64) {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&attn_umma_kernel<128, false, true>), smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_umma_kernel<128, false, true>, dim3(grid), dim3(kUmmaAttnThreads), smem, st, kv_map,
+                      q_map, p);
+  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&attn_umma_kernel<128, false>), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_umma_kernel<128, false>, dim3(grid), dim3(kUmmaAttnThreads), smem, st, kv_map, q_map, p);
 }

@@ -105,7 +105,7 @@ __device__ __forceinline__ float quantize_q_row(const uint8_t* qb16, int half_by
   return exp2f(static_cast<float>(e));
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPREAD = false>
 __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
     attn_umma_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ AttnParams p) {
@@ -113,11 +113,12 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
   // one page of K (or V) for one head: 32 KB of bf16, or 16 KB of E4M3 used as
   // it is by kind::f8f6f4 UMMAs (Q and P then also E4M3)
   constexpr int KV = FP8 ? kGroups * kBox : kGroups * 2 * kBox;
-  // bf16 tiles of at most 64 rows use M = 64 UMMAs, whose accumulator (and
+  // SPREAD (bf16 tiles of 33..64 rows): M = 64 UMMAs, whose accumulator (and
   // TMEM A operand) row m sits in lane 32 (m / 16) + m % 16: 16 rows in every
   // lane quadrant, so the softmax runs on all four SM sub-partitions (a warp
   // reaches only its own quadrant's lanes) at the cost of an M = 128 UMMA.
-  const bool spread = !FP8 && p.rows_pad == 64;
+  static_assert(!(SPREAD && FP8), "the spread layout is for bf16 tiles");
+  constexpr bool spread = SPREAD;
   const uint32_t IDESC_QK = FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(spread ? 64 : 128, 128);
   const uint32_t IDESC_PV = (FP8 ? umma_idesc_e4m3(128, 128) : umma_idesc_bf16(spread ? 64 : 128, 128)) |
                             (1u << 16);  // B (V) MN-major
@@ -447,6 +448,209 @@ __global__ void __launch_bounds__(kUmmaAttnThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&qcv[qb]);
+      }
+    } else if (SPREAD) {
+      // --------------------------- softmax and epilogue, 64-row bf16 tiles
+      // Rows 16q .. 16q + 15 sit in TMEM lanes 32q .. 32q + 15.  The 16-lane
+      // load shape gives thread t two rows, ra = 16q + t / 4 and rb = ra + 8,
+      // and of every 8-column chunk the columns 2 (t % 4) and + 1, so all 32
+      // threads of the warp hold live values; a row's four threads reduce its
+      // maximum and sum with two shuffles.  P goes back with the 16x128b
+      // shape: the positions 2c, 2c + 1 a thread holds are exactly packed P
+      // column c of its rows.
+      const int g4 = lane >> 2, u4 = lane & 3;
+      const int ra = 16 * q + g4, rb = ra + 8;
+      const int ta = ra / G, tb = rb / G;
+      const bool va = ta < T, vb = tb < T;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      float* xmax = ml + 512;  // [2 pages][2 halves][128 rows]
+      float* xl = ml + 1024;   // [2 halves][128 rows]
+      bool dead = false;
+      int it = 0;
+      for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
+           (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
+           cursor_next(cur, scan, nitems, Hk, sparse)) {
+        const int L = Lc;
+        {  // the next sequence's kv_len loads a whole sequence ahead of its use
+          SeqCursor nx = cur;
+          cursor_next(nx, scan, nitems, Hk, sparse);
+          if ((sparse ? nx.s : nx.b) < nitems) Lc = p.kv_lens[nx.b];
+        }
+        const int bound_a = va ? L - T + ta : -1, bound_b = vb ? L - T + tb : -1;
+        const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
+        const float scale = p.scale_log2;
+        float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
+        for (int64_t j = j0; j < j1; ++j, ++it) {
+          const int buf = it % kSBufs;
+          int blk = static_cast<int>(j);
+          uint32_t tokmask = 0xffffffffu;
+          if (sparse) {  // the page's plan entry, loaded 32 to 64 pages ahead
+            if (it > 0 && (it & 31) == 0) plan_ahead_step(qa, p, lane, scan, nitems, Hk, u0, u1);
+            blk = __shfl_sync(0xffffffffu, qa.blk_now, it & 31);
+            tokmask = __shfl_sync(0xffffffffu, qa.m_now, it & 31);
+          }
+          if (!dead)
+            dead = __any_sync(0xffffffffu, !mbar_wait(&sfull[buf], static_cast<uint32_t>(it / kSBufs) & 1u, wt));
+          tc_fence_after();
+          const int pos0 = blk * kPage + hf * 64 + 2 * u4;  // this thread's first position
+          const int bnda = (va && ((tokmask >> ta) & 1u)) ? bound_a : -1;
+          const int bndb = (vb && ((tokmask >> tb) & 1u)) ? bound_b : -1;
+          const bool masked = sparse || blk * kPage + kPage - 1 > L - T;
+          uint32_t sv[32];
+          tmem_ld16x256_x8(tl + buf * 128 + hf * 64, sv);
+          tmem_ld_wait_dep(sv);
+          float xa[16], xb[16];
+          float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int pos = pos0 + 8 * k + e;
+              float a = __uint_as_float(sv[4 * k + e]) * scale;
+              float b = __uint_as_float(sv[4 * k + 2 + e]) * scale;
+              if (masked && pos > bnda) a = -INFINITY;
+              if (masked && pos > bndb) b = -INFINITY;
+              xa[2 * k + e] = a;
+              xb[2 * k + e] = b;
+              mxa = fmaxf(mxa, a);
+              mxb = fmaxf(mxb, b);
+            }
+          mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+          mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+          mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+          mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+          if (u4 == 0) {
+            xmax[((it & 1) * 2 + hf) * 128 + ra] = mxa;
+            xmax[((it & 1) * 2 + hf) * 128 + rb] = mxb;
+          }
+          named_barrier(2 + q, 64);
+          mxa = fmaxf(mxa, xmax[((it & 1) * 2 + (hf ^ 1)) * 128 + ra]);
+          mxb = fmaxf(mxb, xmax[((it & 1) * 2 + (hf ^ 1)) * 128 + rb]);
+          const float mna = fmaxf(ma, mxa), mnb = fmaxf(mb, mxb);
+          const bool needa = ma != -INFINITY && mna > ma + kRescaleLog2;
+          const bool needb = mb != -INFINITY && mnb > mb + kRescaleLog2;
+          if (ma == -INFINITY) ma = mna;
+          if (mb == -INFINITY) mb = mnb;
+          if (__any_sync(0xffffffffu, needa || needb)) {
+            // O must be stable: PV of the previous page has retired
+            const int pv = it - 1;
+            if (!dead)
+              dead = __any_sync(0xffffffffu,
+                                !mbar_wait(&pvdone[pv % kSBufs], static_cast<uint32_t>(pv / kSBufs) & 1u, wt));
+            tc_fence_after();
+            const float aa = needa ? fast_exp2(ma - mna) : 1.f, ab = needb ? fast_exp2(mb - mnb) : 1.f;
+            if (needa) {
+              la *= aa;
+              ma = mna;
+            }
+            if (needb) {
+              lb *= ab;
+              mb = mnb;
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+              uint32_t w[16];
+              tmem_ld16x256_x4(tl + TM_O + hf * 64 + c0, w);
+              tmem_ld_wait_dep(w);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                w[4 * k] = __float_as_uint(__uint_as_float(w[4 * k]) * aa);
+                w[4 * k + 1] = __float_as_uint(__uint_as_float(w[4 * k + 1]) * aa);
+                w[4 * k + 2] = __float_as_uint(__uint_as_float(w[4 * k + 2]) * ab);
+                w[4 * k + 3] = __float_as_uint(__uint_as_float(w[4 * k + 3]) * ab);
+              }
+              tmem_st16x256_x4(tl + TM_O + hf * 64 + c0, w);
+            }
+            tmem_st_wait();
+          }
+          const bool nonea = ma == -INFINITY, noneb = mb == -INFINITY;
+          uint32_t pw[16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float a0 = nonea ? 0.f : fast_exp2(xa[2 * k] - ma);
+            const float a1 = nonea ? 0.f : fast_exp2(xa[2 * k + 1] - ma);
+            const float b0 = noneb ? 0.f : fast_exp2(xb[2 * k] - mb);
+            const float b1 = noneb ? 0.f : fast_exp2(xb[2 * k + 1] - mb);
+            la += a0 + a1;
+            lb += b0 + b1;
+            __nv_bfloat162 pa2 = __floats2bfloat162_rn(a0, a1), pb2 = __floats2bfloat162_rn(b0, b1);
+            pw[2 * k] = *reinterpret_cast<uint32_t*>(&pa2);
+            pw[2 * k + 1] = *reinterpret_cast<uint32_t*>(&pb2);
+          }
+          tmem_st16x128_x8(tl + buf * 128 + hf * 32, pw);
+          tmem_st_wait();
+          // V rows at or past kv_len may hold anything (NaN included): P is
+          // zero there, but 0 * NaN is not, so warp 0 zeroes them first.
+          const int nvalid = L - blk * kPage;
+          if (warp == 0 && nvalid < kPage) {
+            const int vs = it % NV;
+            if (!dead)
+              dead = __any_sync(0xffffffffu, !mbar_wait(&vfull[vs], static_cast<uint32_t>(it / NV) & 1u, wt));
+            uint8_t* vst = vring + vs * KV;
+            const int nchunks = (kPage - nvalid) * 16;
+            for (int idx = lane; idx < nchunks; idx += 32) {
+              const int tok = nvalid + idx / 16, part = idx % 16;
+              *reinterpret_cast<uint4*>(vst + ((part >> 3) * kGroups + tok / kSub) * kBox + (tok % kSub) * 128 +
+                                        (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pfull[buf]);
+        }
+        // ----------------------------------------------------- sequence end
+        const int last = it - 1;
+        if (!dead)
+          dead = __any_sync(0xffffffffu,
+                            !mbar_wait(&pvdone[last % kSBufs], static_cast<uint32_t>(last / kSBufs) & 1u, wt));
+        tc_fence_after();
+        const bool whole = seq_whole(cur, u0, u1, p.setup);
+        const int64_t slot = seq_slot(cur, u0, p.setup);
+        la += __shfl_xor_sync(0xffffffffu, la, 1);
+        lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+        la += __shfl_xor_sync(0xffffffffu, la, 2);
+        lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+        if (u4 == 0) {
+          xl[hf * 128 + ra] = la;
+          xl[hf * 128 + rb] = lb;
+        }
+        named_barrier(2 + q, 64);
+        const float lta = la + xl[(hf ^ 1) * 128 + ra], ltb = lb + xl[(hf ^ 1) * 128 + rb];
+        const float inva = lta > 0.f ? 1.f / lta : 0.f, invb = ltb > 0.f ? 1.f / ltb : 0.f;
+        const float sca = whole ? inva * p.v_scale : inva, scb = whole ? invb * p.v_scale : invb;
+        uint32_t ov[32];
+        tmem_ld16x256_x8(tl + TM_O + hf * 64, ov);
+        tmem_ld_wait_dep(ov);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {  // rows ra, rb
+          const int row = h2 ? rb : ra, tt = h2 ? tb : ta;
+          const float sc = h2 ? scb : sca;
+          if (!(h2 ? vb : va)) continue;
+          const int64_t orow = ((static_cast<int64_t>(cur.b) * T + tt) * p.num_q_heads +
+                                static_cast<int64_t>(cur.h) * G + row % G) * D + hf * 64 + 2 * u4;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float o0 = __uint_as_float(ov[4 * k + 2 * h2]) * sc;
+            const float o1 = __uint_as_float(ov[4 * k + 2 * h2 + 1]) * sc;
+            if (whole) {
+              if (p.out_f32) {
+                *reinterpret_cast<float2*>(static_cast<float*>(p.out) + orow + 8 * k) = make_float2(o0, o1);
+              } else {
+                __nv_bfloat162 pk = __floats2bfloat162_rn(o0, o1);
+                *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + orow + 8 * k) = pk;
+              }
+            } else {
+              *reinterpret_cast<float2*>(p.ws_o + (slot * p.rows_pad + row) * D + hf * 64 + 2 * u4 + 8 * k) =
+                  make_float2(o0, o1);
+            }
+          }
+          if (!whole && hf == 0 && u4 == 0) {
+            const float lt = h2 ? ltb : lta, m = h2 ? mb : ma;
+            p.ws_lse[slot * p.rows_pad + row] = lt > 0.f ? m + __log2f(lt) : -INFINITY;
+          }
+        }
+        tc_fence_before();
       }
     } else {
     const int r = 32 * q + lane;                                   // this thread's TMEM lane
