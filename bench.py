@@ -342,15 +342,15 @@ def time_flat(name, steps, warmup):
 
 
 def time_msa_fused(name, steps, warmup):
-    """The MSA pass with proxy and top-k in one call (trtv_msa_select, the
-    top-k fused into the proxy kernel) followed by the sparse attention: the
-    step time, and the select call on its own."""
+    """The MSA pass as one call (trtv_msa_verify: the top-k fused into the
+    proxy kernel, which also builds the sparse plan, then the attention): the
+    step time, and the select call (trtv_msa_select) on its own."""
     import torch
     from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
     p = make(name)
     dv = DeviceVerify(p)
     out = {}
-    for label, calls in (("step", [dv.select_fused, dv.sparse]), ("select", [dv.select_fused])):
+    for label, calls in (("step", [dv.msa_verify]), ("select", [dv.select_fused])):
         for _ in range(warmup):
             for f in calls:
                 f()
@@ -363,7 +363,7 @@ def time_msa_fused(name, steps, warmup):
         e.record()
         torch.cuda.synchronize()
         out[label + "_ms"] = s.elapsed_time(e) / steps
-    out["launches_per_step"] = 4   # proxy with fused top-k, sparse plan, attention, combine
+    out["launches_per_step"] = 4   # counter zeroing, proxy with fused top-k and plan, attention, combine
     from speculative_decode_verify_kv_gb300 import trtv_get_device_error
     out["device_error"] = trtv_get_device_error()
     del dv

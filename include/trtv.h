@@ -207,8 +207,8 @@ trtv_status trtv_msa_topk(const trtv_geom* geom, const float* scores, const int3
  *   scores     fp32 [B, T, Hk, max_pages] (written, as trtv_msa_proxy_score)
  *   block_idx  int32 [B, T, Hk, topk] (written, as trtv_msa_topk)
  *   workspace  >= trtv_workspace_bytes(geom, topk) bytes, 256-byte aligned; a
- *              per-sequence page counter in it is zeroed by an asynchronous
- *              memset on `stream` before the kernel (no initial contents
+ *              per-sequence page counter in it is zeroed by a small kernel
+ *              on `stream` before the proxy kernel (no initial contents
  *              needed).  1 <= topk <= 1024.
  * Errors as trtv_msa_proxy_score and trtv_msa_topk, plus TRTV_ERR_WORKSPACE.
  */
@@ -230,6 +230,28 @@ trtv_status trtv_msa_sparse_attn(const trtv_geom* geom, const void* q, const voi
                                  const int32_t* block_idx, int32_t topk, void* out,
                                  int32_t out_dtype, void* workspace, size_t ws_bytes,
                                  void* stream);
+
+/*
+ * The whole MSA verify step in one call (source: PR #3 "... verify" commit:
+ * proxy scores, per-token top-k, sparse attention over the selected blocks):
+ * the results of trtv_msa_select followed by trtv_msa_sparse_attn with the
+ * same block_idx and topk.  When the fused select applies (see
+ * trtv_msa_select) and max_pages_per_req <= 2032, the CTA that selects a
+ * (request, KV head) sequence's blocks also builds the sequence's sparse plan
+ * (its unique blocks, the tokens that chose each, their page slots) in the
+ * workspace, and the attention runs from it: no plan kernel and no top-k
+ * kernel are launched.
+ *   scores     fp32 [B, T, Hk, max_pages] (written)
+ *   block_idx  int32 [B, T, Hk, topk] (written)
+ *   out        as trtv_msa_sparse_attn (written)
+ *   workspace  >= trtv_workspace_bytes(geom, topk) bytes, 256-byte aligned,
+ *              no initial contents needed.  1 <= topk <= 1024.
+ * Errors as trtv_msa_select and trtv_msa_sparse_attn.
+ */
+trtv_status trtv_msa_verify(const trtv_geom* geom, const void* q, const void* kv_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, int32_t topk,
+                            float* scores, int32_t* block_idx, void* out, int32_t out_dtype,
+                            void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * KV slot staging along the ladder (source: PR #3 "... verify" commit: "KV

@@ -21,8 +21,8 @@ __all__ = [
     "trtv_msa_topk", "trtv_msa_sparse_attn", "trtv_get_device_error", "trtv_version",
     "trtv_verify_dense_noalloc", "trtv_stage_kv", "trtv_flatten_page_table",
     "trtv_page_table_from_flat", "trtv_workspace_bytes_flat", "trtv_verify_dense_flat",
-    "trtv_draft_attn_p32", "trtv_msa_select", "trtv_status_string", "trtv_test_withhold_pages",
-    "geom_of", "EXPORTS",
+    "trtv_draft_attn_p32", "trtv_msa_select", "trtv_msa_verify", "trtv_status_string",
+    "trtv_test_withhold_pages", "geom_of", "EXPORTS",
 ]
 
 TRTV_OK, TRTV_ERR_INVALID_ARG, TRTV_ERR_UNSUPPORTED, TRTV_ERR_CUDA, TRTV_ERR_WORKSPACE = range(5)
@@ -34,7 +34,7 @@ EXPORTS = ("trtv_status_string", "trtv_version", "trtv_subpage_view", "trtv_work
            "trtv_verify_dense", "trtv_verify_dense_noalloc", "trtv_msa_proxy_score", "trtv_msa_topk",
            "trtv_msa_sparse_attn", "trtv_stage_kv", "trtv_flatten_page_table",
            "trtv_page_table_from_flat", "trtv_workspace_bytes_flat", "trtv_verify_dense_flat",
-           "trtv_draft_attn_p32", "trtv_msa_select", "trtv_test_withhold_pages",
+           "trtv_draft_attn_p32", "trtv_msa_select", "trtv_msa_verify", "trtv_test_withhold_pages",
            "trtv_get_device_error")
 
 
@@ -108,6 +108,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     h.trtv_draft_attn_p32.argtypes = [G, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
     h.trtv_msa_select.restype = ctypes.c_int
     h.trtv_msa_select.argtypes = [G, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    h.trtv_msa_verify.restype = ctypes.c_int
+    h.trtv_msa_verify.argtypes = [G, vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, sz, vp]
     h.trtv_get_device_error.restype = ctypes.c_int
     h.trtv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
     h.trtv_test_withhold_pages.restype = ctypes.c_int
@@ -206,6 +208,15 @@ def trtv_msa_select(geom: Geom, q, kv_pool, page_table, kv_lens, topk: int, scor
     _check("trtv_msa_select", load().trtv_msa_select(
         ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens), topk,
         _ptr(scores), _ptr(block_idx), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def trtv_msa_verify(geom: Geom, q, kv_pool, page_table, kv_lens, topk: int, scores, block_idx, out,
+                    out_dtype: int, workspace, ws_bytes: int, stream=None) -> None:
+    """Proxy scores, per-token top-k and sparse attention in one call (the
+    fused select builds the sparse plan where it applies)."""
+    _check("trtv_msa_verify", load().trtv_msa_verify(
+        ctypes.byref(geom), _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(kv_lens), topk,
+        _ptr(scores), _ptr(block_idx), _ptr(out), out_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def trtv_msa_sparse_attn(geom: Geom, q, kv_pool, page_table, kv_lens, block_idx, topk: int, out,

@@ -170,6 +170,17 @@ trtv_status make_plan(const trtv_geom* g, int topk, Plan* pl) {
   return TRTV_OK;
 }
 
+// The sparse plan's regions of the workspace (slots only with a page table).
+PlanOut plan_out(const Plan& pl, uint8_t* wsb, bool slots) {
+  PlanOut o;
+  o.blocks = reinterpret_cast<int32_t*>(wsb + pl.ws_blocks);
+  o.masks = reinterpret_cast<uint32_t*>(wsb + pl.ws_masks);
+  o.count = reinterpret_cast<int32_t*>(wsb + pl.ws_count);
+  o.slots = slots ? reinterpret_cast<int32_t*>(wsb + pl.ws_slots) : nullptr;
+  o.cap = pl.plan_cap;
+  return o;
+}
+
 bool encode_pool_map(const trtv_geom* g, const Plan& pl, const void* pool, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (enc == nullptr) return false;
@@ -443,9 +454,11 @@ bool flat_geometry_ok(const trtv_geom* g) {
          g->batch <= 65536;
 }
 
+// plan_ready (sparse): the workspace already holds this call's sparse plan
+// (the fused select built it), so the plan kernel is skipped.
 trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, const KvIndex& kvi,
                         const int32_t* lens, const int32_t* block_idx, int topk, void* out,
-                        int32_t out_dtype, void* ws, size_t ws_bytes, void* stream) {
+                        int32_t out_dtype, void* ws, size_t ws_bytes, void* stream, bool plan_ready = false) {
   const bool sparse = block_idx != nullptr;
   const bool p32 = kvi.k_sub != nullptr || kvi.v_sub != nullptr;
   Plan pl;
@@ -525,13 +538,9 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
                           nullptr, err, st);
     if (e != cudaSuccess) return TRTV_ERR_CUDA;
   }
-  if (sparse) {
-    e = launch_sparse_plan(block_idx, lens, g->batch, g->qo_len, g->num_kv_heads,
-                           g->max_pages_per_req, topk, pl.plan_cap,
-                           reinterpret_cast<int32_t*>(wsb + pl.ws_blocks),
-                           reinterpret_cast<uint32_t*>(wsb + pl.ws_masks),
-                           reinterpret_cast<int32_t*>(wsb + pl.ws_count), a.page_table, g->num_slots,
-                           const_cast<int32_t*>(a.plan_slots), err, st);
+  if (sparse && !plan_ready) {
+    e = launch_sparse_plan(block_idx, lens, g->batch, g->qo_len, g->num_kv_heads, g->max_pages_per_req, topk,
+                           plan_out(pl, wsb, !p32), a.page_table, g->num_slots, err, st);
     if (e != cudaSuccess) return TRTV_ERR_CUDA;
   }
   e = pm     ? launch_attn_pm(g->kv_dtype == TRTV_FP8_E4M3, pl.rows_pad, map, qmap, a, pl.num_ctas, smem, st)
@@ -646,9 +655,14 @@ namespace {
 // Proxy scores, and with block_idx set the per-token top-k as well: fused
 // into the tcgen05 proxy kernel when that kernel applies (the sequence
 // counters in the workspace zeroed first), else the top-k kernel after it.
+// planned (optional): when set and the fused kernel applies with at most
+// kFusedPlanMaxPages pages per request, the fused kernel also builds the
+// sparse plan in the workspace and *planned is set.
+constexpr int kFusedPlanMaxPages = 2032;  // the plan's mask fits the histogram scratch
 trtv_status proxy_common(const trtv_geom* g, const void* q, const void* kv_pool, const int32_t* page_table,
                          const int32_t* kv_lens, float* scores, int32_t topk, int32_t* block_idx, void* ws,
-                         size_t ws_bytes, void* stream) {
+                         size_t ws_bytes, void* stream, bool* planned = nullptr) {
+  if (planned != nullptr) *planned = false;
   const bool select = block_idx != nullptr;
   Plan pl;
   trtv_status s = make_plan(g, select ? topk : 0, &pl);
@@ -700,8 +714,11 @@ trtv_status proxy_common(const trtv_geom* g, const void* q, const void* kv_pool,
     a.topk_out = block_idx;
     a.topk = topk;
     a.seq_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + pl.ws_sel);
-    if (cudaMemsetAsync(a.seq_count, 0, static_cast<size_t>(pl.n_seq) * sizeof(int32_t), st) != cudaSuccess)
-      return TRTV_ERR_CUDA;
+    if (launch_zero(a.seq_count, pl.n_seq, st) != cudaSuccess) return TRTV_ERR_CUDA;
+    if (planned != nullptr && g->max_pages_per_req <= kFusedPlanMaxPages) {
+      a.plan = plan_out(pl, static_cast<uint8_t*>(ws), true);
+      *planned = true;
+    }
   }
   cudaError_t e = umma ? launch_proxy_umma(map, qmap, a, pl.num_ctas, smem, st)
                        : g->kv_dtype == TRTV_FP8_E4M3
@@ -727,6 +744,18 @@ trtv_status trtv_msa_select(const trtv_geom* g, const void* q, const void* kv_po
   if (block_idx == nullptr) return TRTV_ERR_INVALID_ARG;
   return proxy_common(g, q, kv_pool, page_table, kv_lens, scores, topk, block_idx, workspace, ws_bytes,
                       stream);
+}
+
+trtv_status trtv_msa_verify(const trtv_geom* g, const void* q, const void* kv_pool, const int32_t* page_table,
+                            const int32_t* kv_lens, int32_t topk, float* scores, int32_t* block_idx, void* out,
+                            int32_t out_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (block_idx == nullptr) return TRTV_ERR_INVALID_ARG;
+  bool planned = false;
+  const trtv_status s = proxy_common(g, q, kv_pool, page_table, kv_lens, scores, topk, block_idx, workspace,
+                                     ws_bytes, stream, &planned);
+  if (s != TRTV_OK) return s;
+  return attn_common(g, q, kv_pool, KvIndex{page_table, nullptr, nullptr, nullptr}, kv_lens, block_idx, topk, out,
+                     out_dtype, workspace, ws_bytes, stream, planned);
 }
 
 trtv_status trtv_msa_topk(const trtv_geom* g, const float* scores, const int32_t* kv_lens,

@@ -41,6 +41,16 @@ constexpr int kUmmaSeqSetup = 1;   // tcgen05 attention
 // and the workspace slot offset of the first piece; b = -1 when the boundary
 // starts no cut.  Written by the attention CTA that starts at the boundary,
 // read by the split-combine kernel.
+// Where a sparse plan goes (plan.cuh): ascending unique blocks, token masks
+// and page slots of every (request, KV head) sequence, and their counts.
+struct PlanOut {
+  int32_t* blocks;    // [n_seq, cap]
+  uint32_t* masks;    // [n_seq, cap]
+  int32_t* count;     // [n_seq]
+  int32_t* slots;     // [n_seq, cap] or null
+  int cap;
+};
+
 struct SplitDesc {
   int b, h, c_first, nc, first_off, pad;
   long long W;  // total units of the call
@@ -107,6 +117,9 @@ struct ProxyParams {
   int32_t* topk_out;
   int32_t* seq_count;
   int topk;
+  // with topk_out: when plan.count is set, that CTA also builds the sequence's
+  // sparse plan (plan.cuh) in the histogram scratch (max_pages <= 2032)
+  PlanOut plan;
   uint64_t wait_ns;     // as in AttnParams
   int withhold;
 };

@@ -9,6 +9,10 @@ namespace trtv {
 
 struct AttnParams;
 struct ProxyParams;
+struct PlanOut;
+
+// n int32 counters set to 0 on `st` (a kernel in the programmatic launch chain)
+cudaError_t launch_zero(int32_t* c, int n, cudaStream_t st);
 
 // attention: head_dim in {64, 128}; mt (row tiles of 16) in {1, 2, 4, 8}
 cudaError_t launch_attn_bf16(int head_dim, int mt, const CUtensorMap& map, const AttnParams& p,
@@ -43,10 +47,8 @@ cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t*
                                 int32_t* v_sub, int batch, int qo_len, int max_pages,
                                 int num_slots, int stride, int* err, cudaStream_t st);
 cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
-                               int num_kv_heads, int max_pages, int topk, int plan_cap,
-                               int32_t* plan_blocks, uint32_t* plan_masks, int32_t* plan_count,
-                               const int32_t* pt, int num_slots, int32_t* plan_slots, int* err,
-                               cudaStream_t st);
+                               int num_kv_heads, int max_pages, int topk, const PlanOut& out,
+                               const int32_t* pt, int num_slots, int* err, cudaStream_t st);
 cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int qo_len,
                         int num_kv_heads, int max_pages, int topk, int32_t* out, int* err,
                         cudaStream_t st);

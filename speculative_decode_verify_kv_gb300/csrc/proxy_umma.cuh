@@ -27,11 +27,13 @@
 // Fused top-k (topk_out set): at the end of each sequence it touched, the CTA
 // adds its page count to the sequence's counter; the CTA that completes the
 // count selects the top-k blocks of the sequence's qo_len rows (topk_row, one
-// epilogue warp per row) from the scores every contributor wrote.  Requests
-// with no pages get rows of -1 from CTA b % grid.
+// epilogue warp per row) from the scores every contributor wrote, and (plan
+// set) the sequence's sparse plan from those rows.  Requests with no pages get
+// rows of -1 (and empty plans) from CTA b % grid.
 #pragma once
 
 #include "attn.cuh"
+#include "plan.cuh"
 #include "topk.cuh"
 #include "umma.cuh"
 
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
       if (scan[b + 1] != scan[b]) continue;
       int32_t* o = p.topk_out + static_cast<int64_t>(b) * T * Hk * p.topk;
       for (int e = threadIdx.x; e < T * Hk * p.topk; e += blockDim.x) o[e] = -1;
+      if (p.plan.count != nullptr)
+        for (int h = threadIdx.x; h < Hk; h += blockDim.x) p.plan.count[b * Hk + h] = 0;
     }
   }
   if (W == 0) return;
@@ -288,6 +292,14 @@ __global__ void __launch_bounds__(kUmmaProxyThreads, 1)
             const int64_t row = (static_cast<int64_t>(cur.b) * T + tt) * Hk + cur.h;
             topk_row(p.scores + row * NP, (L - T + tt) / kPage + 1, p.topk, p.topk_out + row * p.topk,
                      reinterpret_cast<uint32_t*>(smem + p.off_red) + warp * 256, lane);
+          }
+          if (p.plan.count != nullptr) {
+            // the sequence's rows are written: its plan, in the histogram scratch
+            uint32_t* scratch = reinterpret_cast<uint32_t*>(smem + p.off_red);
+            named_barrier(1, 256);
+            build_sequence_plan(p.topk_out, cur.b, cur.h, T, Hk, p.topk, NP, L, p.plan, p.page_table, p.num_slots,
+                                p.err, scratch, scratch + 2039, reinterpret_cast<int32_t*>(scratch) + 2040,
+                                threadIdx.x, 256, [] { named_barrier(1, 256); });
           }
         }
         named_barrier(1, 256);  // seq_last is rewritten for the next sequence

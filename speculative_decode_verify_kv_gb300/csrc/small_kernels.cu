@@ -13,6 +13,7 @@
 //                         from the lengths
 #include "common.cuh"
 #include "launch.h"
+#include "plan.cuh"
 #include "topk.cuh"
 
 namespace trtv {
@@ -49,93 +50,37 @@ __global__ void subpage_view_kernel(const int32_t* __restrict__ pt, const int32_
 }
 
 // ---------------------------------------------------------------------------
-// Sparse plan ("Eagle3 for M3 MSA path + CUDA graphs compatibility", verify
-// commit: the sparse pass consumes per-row selected blocks).  For sequence
-// (b, h): mask[v] = bitmask of tokens t whose list selected block v; a token
-// whose list holds an index >= max_pages selects nothing (its rows are zero)
-// and raises TRTV_DEVERR_BLOCK_IDX; blocks at or past kv_len are dropped
-// (no token sees them).  Output: ascending unique blocks with their masks,
-// and (given the page table `pt`) each block's slot, a slot outside the pool
-// raising TRTV_DEVERR_PAGE_ID and reading as slot 0.
+// Zeroes n counters once the previous kernel of the stream has finished (a
+// kernel, unlike a memset, keeps the launch chain programmatic, so the kernel
+// after it is set up while this one runs).
+__global__ void zero_kernel(int32_t* __restrict__ c, int n) {
+  pdl_trigger();
+  pdl_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) c[i] = 0;
+}
+
+cudaError_t launch_zero(int32_t* c, int n, cudaStream_t st) {
+  const int threads = 256;
+  const int blocks = n / threads + 1 < 64 ? n / threads + 1 : 64;
+  return launch_pdl(zero_kernel, dim3(blocks), dim3(threads), 0, st, c, n);
+}
+
+// ---------------------------------------------------------------------------
+// Sparse plan: one CTA per (request, KV head) sequence builds its plan
+// (build_sequence_plan, plan.cuh) from the sequence's T rows of selected
+// blocks.
 __global__ void sparse_plan_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ lens,
                                    int batch, int qo_len, int num_kv_heads, int max_pages, int topk,
-                                   int plan_cap, int32_t* __restrict__ plan_blocks,
-                                   uint32_t* __restrict__ plan_masks, int32_t* __restrict__ plan_count,
-                                   const int32_t* __restrict__ pt, int num_slots,
-                                   int32_t* __restrict__ plan_slots, int* err) {
+                                   PlanOut out, const int32_t* __restrict__ pt, int num_slots, int* err) {
   extern __shared__ uint32_t mask[];  // [max_pages]
   __shared__ uint32_t bad_tokens;
   __shared__ int32_t warp_tot[32];
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, b = s / num_kv_heads, h = s % num_kv_heads;
-  const int T = qo_len, L = lens[b];
-  if (!len_valid(L, T, max_pages)) {
-    if (threadIdx.x == 0) {
-      plan_count[s] = 0;
-      if (h == 0) atomicOr(err, TRTV_DEVERR_KV_LEN);
-    }
-    return;
-  }
-  const int npages = (L + kPage - 1) / kPage;
-  for (int i = threadIdx.x; i < npages; i += blockDim.x) mask[i] = 0;
-  if (threadIdx.x == 0) bad_tokens = 0;
-  __syncthreads();
-  for (int e = threadIdx.x; e < T * topk; e += blockDim.x) {
-    const int t = e / topk, i = e % topk;
-    const int v = idx[((static_cast<int64_t>(b) * T + t) * num_kv_heads + h) * topk + i];
-    if (v < 0) continue;
-    if (v >= max_pages) {
-      atomicOr(&bad_tokens, 1u << t);
-      atomicOr(err, TRTV_DEVERR_BLOCK_IDX);
-      continue;
-    }
-    if (v >= npages) continue;
-    atomicOr(&mask[v], 1u << t);
-  }
-  __syncthreads();
-  const uint32_t keep_bits = ~bad_tokens;
-  // ordered compaction: each thread a contiguous segment
-  const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int seg = (npages + nthr - 1) / nthr;
-  const int lo = min(npages, tid * seg), hi = min(npages, lo + seg);
-  int local = 0;
-  for (int i = lo; i < hi; ++i) local += (mask[i] & keep_bits) != 0;
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int w = 0; w < (nthr + 31) / 32; ++w) {
-      const int t = warp_tot[w];
-      warp_tot[w] = run;
-      run += t;
-    }
-    plan_count[s] = run;
-  }
-  __syncthreads();
-  int pos = warp_tot[warp] + incl - local;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t m = mask[i] & keep_bits;
-    if (m != 0) {
-      plan_blocks[static_cast<int64_t>(s) * plan_cap + pos] = i;
-      plan_masks[static_cast<int64_t>(s) * plan_cap + pos] = m;
-      if (pt != nullptr) {
-        int slot = pt[static_cast<int64_t>(b) * max_pages + i];
-        if (slot < 0 || slot >= num_slots) {
-          atomicOr(err, TRTV_DEVERR_PAGE_ID);
-          slot = 0;
-        }
-        plan_slots[static_cast<int64_t>(s) * plan_cap + pos] = slot;
-      }
-      ++pos;
-    }
-  }
+  build_sequence_plan(idx, b, h, qo_len, num_kv_heads, topk, max_pages, lens[b], out, pt, num_slots, err, mask,
+                      &bad_tokens, warp_tot, threadIdx.x, blockDim.x, [] { __syncthreads(); });
+  (void)batch;
 }
 
 // ---------------------------------------------------------------------------
@@ -447,10 +392,8 @@ cudaError_t launch_subpage_view(const int32_t* pt, const int32_t* lens, int32_t*
 }
 
 cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batch, int qo_len,
-                               int num_kv_heads, int max_pages, int topk, int plan_cap,
-                               int32_t* plan_blocks, uint32_t* plan_masks, int32_t* plan_count,
-                               const int32_t* pt, int num_slots, int32_t* plan_slots, int* err,
-                               cudaStream_t st) {
+                               int num_kv_heads, int max_pages, int topk, const PlanOut& out,
+                               const int32_t* pt, int num_slots, int* err, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(max_pages) * sizeof(uint32_t);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(sparse_plan_kernel,
@@ -459,8 +402,7 @@ cudaError_t launch_sparse_plan(const int32_t* idx, const int32_t* lens, int batc
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(sparse_plan_kernel, dim3(batch * num_kv_heads), dim3(256), smem, st, idx, lens, batch,
-                    qo_len, num_kv_heads, max_pages, topk, plan_cap, plan_blocks, plan_masks, plan_count,
-                    pt, num_slots, plan_slots, err);
+                    qo_len, num_kv_heads, max_pages, topk, out, pt, num_slots, err);
 }
 
 cudaError_t launch_topk(const float* scores, const int32_t* lens, int batch, int qo_len,

@@ -15,7 +15,7 @@ from typing import Optional
 import torch
 
 from . import (TRTV_BF16, TRTV_F32, geom_of, trtv_draft_attn_p32, trtv_flatten_page_table,
-               trtv_msa_proxy_score, trtv_msa_select, trtv_msa_sparse_attn, trtv_msa_topk,
+               trtv_msa_proxy_score, trtv_msa_select, trtv_msa_sparse_attn, trtv_msa_topk, trtv_msa_verify,
                trtv_page_table_from_flat,
                trtv_stage_kv, trtv_subpage_view, trtv_verify_dense, trtv_verify_dense_flat,
                trtv_workspace_bytes, trtv_workspace_bytes_flat)
@@ -85,6 +85,12 @@ class DeviceVerify:
                         self.scores, self.block_idx, self.workspace, self.ws_bytes, stream)
         return self.block_idx
 
+    def msa_verify(self, stream=None):
+        """Proxy scores, top-k and sparse attention in one call (trtv_msa_verify)."""
+        trtv_msa_verify(self.geom, self.q, self.pool, self.page_table, self.kv_lens, self.topk, self.scores,
+                        self.block_idx, self.out, self.out_dtype, self.workspace, self.ws_bytes, stream)
+        return self.out
+
     def sparse(self, block_idx=None, topk: Optional[int] = None, stream=None):
         idx = self.block_idx if block_idx is None else block_idx
         k = self.topk if topk is None else topk
@@ -131,6 +137,6 @@ class DeviceVerify:
         return self.sparse(stream=stream)
 
     def msa_fused(self, stream=None):
-        """The same pass with proxy and top-k in one call."""
-        self.select_fused(stream)
-        return self.sparse(stream=stream)
+        """The same pass in one call (trtv_msa_verify: fused select building
+        the sparse plan, then the sparse attention)."""
+        return self.msa_verify(stream)

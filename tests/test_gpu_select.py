@@ -1,6 +1,8 @@
 """Proxy scores + per-token top-k in one call (trtv_msa_select) against the
 two-call path and the oracle: scores identical to trtv_msa_proxy_score's,
-indices bit-exact (the oracle's selection run on the GPU's fp32 scores)."""
+indices bit-exact (the oracle's selection run on the GPU's fp32 scores).  The
+whole MSA step in one call (trtv_msa_verify, whose fused select also builds
+the sparse plan) against select + sparse attention: bit-identical."""
 import numpy as np
 import pytest
 import torch
@@ -104,3 +106,34 @@ def test_select_then_sparse_under_graph_replay():
         ref, _ = oracle.sparse_attn(x, idx)
         assert np.abs(dv.out.cpu().numpy() - ref).max() <= 2e-2
         T.trtv_get_device_error()
+
+
+@pytest.mark.parametrize("Hq,Hk,Tq,dtype,num_ctas,max_pages", [
+    (64, 4, 4, W.BF16, 0, 48),      # fused select builds the plan (64 rows)
+    (64, 4, 4, W.BF16, 1, 48),      # one CTA selects and plans every sequence
+    (32, 4, 4, W.BF16, 7, 48),      # 32 rows: position-major attention
+    (16, 2, 8, W.BF16, 150, 48),    # many CTAs per sequence
+    (64, 4, 8, W.BF16, 5, 48),      # 128 rows
+    (64, 4, 4, W.BF16, 0, 2040),    # too many pages per request: plan kernel
+    (32, 4, 4, W.FP8, 5, 48),       # FP8: proxy + top-k kernels + plan kernel
+])
+def test_msa_verify_equals_select_then_sparse(Hq, Hk, Tq, dtype, num_ctas, max_pages):
+    p = W.make_problem(kv_lens=[3000, 129, 2, 5000, 700, 40], qo_len=Tq, num_q_heads=Hq, num_kv_heads=Hk,
+                       head_dim=128, kv_dtype=dtype, seed=Hq + Tq + num_ctas + 5, topk=8,
+                       max_pages_per_req=max_pages, out_dtype="f32")
+    dv = DeviceVerify(p, num_ctas=num_ctas, out_dtype="f32")
+    dv.select_fused()
+    dv.sparse()
+    torch.cuda.synchronize()
+    i2, o2 = dv.block_idx.clone(), dv.out.clone()
+    T.trtv_get_device_error()
+    dv.block_idx.fill_(-7)
+    dv.out.fill_(float("nan"))
+    dv.workspace.fill_(0xAB)  # the one-call path needs no workspace contents
+    dv.msa_verify()
+    torch.cuda.synchronize()
+    assert T.trtv_get_device_error() & T.DEVERR_KV_LEN          # request 2: kv_len < qo_len
+    assert torch.equal(dv.block_idx, i2)
+    assert torch.equal(dv.out, o2)
+    ref, _ = oracle.sparse_attn(oracle.Inputs(p), i2.cpu().numpy())
+    assert np.abs(dv.out.cpu().numpy() - ref).max() <= 2e-2
