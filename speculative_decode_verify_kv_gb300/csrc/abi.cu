@@ -527,7 +527,7 @@ trtv_status attn_common(const trtv_geom* g, const void* q, const void* pool, con
   a.v_scale = g->v_scale;
   // stream-K charge per sequence start, in pages: what a sequence switch costs
   // each kernel relative to one page of K and V
-  a.setup = (pm || umma) ? kUmmaSeqSetup : kSeqSetup;
+  a.setup = pm ? kPmSeqSetup : umma ? kUmmaSeqSetup : kSeqSetup;
   a.lg_group = 0;
   while ((1 << a.lg_group) < pl.group) ++a.lg_group;
   a.wait_ns = g_wait_ns.load();

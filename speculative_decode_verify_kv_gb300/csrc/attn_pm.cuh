@@ -455,10 +455,16 @@ __global__ void __launch_bounds__(pm_threads(FP8, NR), 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     bool dead = false;
     int it = 0, ip = 0, sq = 0;  // pages, pairs and sequences so far
+    int Lc = p.kv_lens[cursor_first(scan, nitems, Hk, sparse, u0).b];  // kv_len of the sequence about to start
     for (SeqCursor cur = cursor_first(scan, nitems, Hk, sparse, u0);
          (sparse ? cur.s : cur.b) < nitems && seq_in_range(cur, u1, p.setup);
          cursor_next(cur, scan, nitems, Hk, sparse), ++sq) {
-      const int L = p.kv_lens[cur.b];
+      const int L = Lc;
+      {  // the next sequence's kv_len loads a whole sequence ahead of its use
+        SeqCursor nx = cur;
+        cursor_next(nx, scan, nitems, Hk, sparse);
+        if ((sparse ? nx.s : nx.b) < nitems) Lc = p.kv_lens[nx.b];
+      }
       const int64_t j0 = seq_j0(cur, u0, p.setup), j1 = seq_j1(cur, u1, p.setup);
       // logit scale per column in the log2 domain (FP8: times the row's Q scale)
       float sc[H];

@@ -32,7 +32,9 @@ constexpr int kUmmaAttnFp8Stages = 6;  // most FP8 K and V pages (16 KB each) pe
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any barrier wait
 // stream-K setup charge per sequence, in units (pages or blocks)
 constexpr int kSeqSetup = 3;       // mma.sync attention
-constexpr int kUmmaSeqSetup = 1;   // tcgen05 attention
+constexpr int kUmmaSeqSetup = 2;   // tcgen05 attention, row-major
+constexpr int kPmSeqSetup = 6;     // tcgen05 attention, position-major (a sequence
+                                   // switch costs about as much as six pages)
 
 // ---- parameter blocks ----------------------------------------------------
 
