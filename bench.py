@@ -244,8 +244,10 @@ def time_path(name, steps, warmup, sampler=None, min_seconds=1.0, max_repeats=20
     only around the K-step loop, which is repeated until `min_seconds` of
     device time (at least once); ms_per_step is the median repeat.  Dominant
     call: the same K-step loop with that call alone (events around the loop),
-    so its time is the call's own share of a step.  Per-call times of every
-    call come from a third, shorter loop with an event after every call."""
+    so its time is the call's own share of a step; every other call is timed
+    alone the same way.  Per-call times of every call inside the step come
+    from a third, shorter loop with an event after every call (which keeps
+    consecutive calls from overlapping, so these are upper bounds)."""
     import torch
     from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
     p = make(name)
@@ -284,6 +286,9 @@ def time_path(name, steps, warmup, sampler=None, min_seconds=1.0, max_repeats=20
         reps.append(ms / steps)
     t1 = time.time()
     dom_reps = [loop([dom_f]) / steps for _ in range(3)]
+    # every call moving KV bytes also timed alone, back to back (median of 3)
+    alone = {n: float(np.median([loop([f]) / steps for _ in range(3)])) for n, f in calls if n != dom}
+    alone[dom] = float(np.median(dom_reps))
     n_pc = max(10, steps // 8)
     ev = [[E() for _ in range(len(calls) + 1)] for _ in range(n_pc)]
     for k in range(n_pc):
@@ -299,6 +304,7 @@ def time_path(name, steps, warmup, sampler=None, min_seconds=1.0, max_repeats=20
     derr = trtv_get_device_error()
     res = {"p": p, "dv": dv, "ms_per_step": float(np.median(reps)), "repeats": len(reps),
            "timed_s": total / 1e3, "dom": dom, "dom_ms": float(np.median(dom_reps)), "per_call_ms": per_call,
+           "alone_ms": alone,
            "t0": t0, "t1": t1, "launches_per_step": launches, "device_error": derr}
     if p.topk:
         idx = dv.block_idx.cpu().numpy()
@@ -589,6 +595,13 @@ def main():
             g = b / (ms_c / 1e3) / 1e9
             calls[n] = [sig(ms_c * 1e3), sig(g), sig(g / peak, 3)]
         dg = r["bytes"][r["dom"]] / (r["dom_ms"] / 1e3) / 1e9
+        alone = {}
+        for n, b in r["bytes"].items():
+            if b < 1e8:  # the KV-streaming calls only
+                continue
+            ms_c = r["alone_ms"][n]
+            g = b / (ms_c / 1e3) / 1e9
+            alone[n] = [sig(ms_c * 1e3), sig(g), sig(g / peak, 3), sig(g / NOMINAL_HBM_GBS, 3)]
         return {"path": name, "workload": describe(pe, name)["workload"],
                 "value": sig(pe.batch * pe.qo_len / (r["ms_per_step"] / 1e3)), "unit": UNIT,
                 "ms_per_step": sig(r["ms_per_step"]), "repeats": r["repeats"],
@@ -596,7 +609,8 @@ def main():
                 "step_frac_of_8tbs": sig(gbs / NOMINAL_HBM_GBS, 3),
                 "dominant": {"call": r["dom"], "us_alone": sig(r["dom_ms"] * 1e3), "gbs": sig(dg),
                              "frac_of_measured": sig(dg / peak, 3), "frac_of_8tbs": sig(dg / NOMINAL_HBM_GBS, 3)},
-                "calls_us_gbs_frac": calls, "device_error": r["device_error"],
+                "calls_us_gbs_frac": calls,
+                "calls_alone_us_gbs_frac_of_measured_frac_of_8tbs": alone, "device_error": r["device_error"],
                 "gpu_launches_per_step": r["launches_per_step"]}
 
     # ---- other workloads first (one short line each), then the headline
