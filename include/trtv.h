@@ -311,7 +311,8 @@ trtv_status trtv_page_table_from_flat(const trtv_geom* geom, const int32_t* flat
 
 /*
  * Dense ladder verify taking the flat table: trtv_page_table_from_flat into
- * the workspace, then trtv_verify_dense on it (two kernels, same stream).
+ * the workspace, then trtv_verify_dense on it (one stream: the table
+ * kernel, then the verify's kernels).
  * Workspace: trtv_workspace_bytes(geom, 0) plus
  * 4 * batch * max_pages_per_req bytes rounded up to 256
  * (trtv_workspace_bytes_flat).

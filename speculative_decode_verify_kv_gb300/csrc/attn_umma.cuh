@@ -10,25 +10,28 @@
 // (K page at slot * stride, V page at slot * stride + 1).
 //
 // Work split as in attn_kernel (stream-K over the pages / selected blocks of
-// every (request, KV head) sequence, in-kernel merge of cut sequences).  Per
-// sequence the (token, group head) rows (row = t * G + g) are the M = 128
-// UMMA tile; per page:
-//   S = Q K^T       8 UMMA 128x128x16 -> TMEM S[buf] (fp32, lane = row)
+// every (request, KV head) sequence; cut sequences are merged by the
+// split-combine kernel).  Per sequence the (token, group head) rows (row =
+// t * G + g) are the UMMA's M -- M = 128, or for tiles of at most 64 bf16 rows
+// M = 64, whose rows sit 16 to a TMEM lane quadrant -- and per page:
+//   S = Q K^T       8 UMMA Mx128x16 -> TMEM S[buf] (fp32, lane = row)
 //   softmax         warps 0-7: warp w reads TMEM lane quadrant w % 4 and
-//                   columns 64 (w / 4) .. + 63 of each row; the two warps of a
-//                   quadrant swap their row maxima through shared memory.
-//                   Online maximum in the log2 domain (O rescaled only when a
-//                   row's maximum rises by more than 8; the stale maximum is
-//                   exact since the final division uses the same one),
-//                   P = 2^(x - m) as bf16 pairs stored back over S[buf]
-//   O += P V        8 UMMA 128x128x16 with A = P in TMEM and B = the V page
+//                   columns 64 (w / 4) .. + 63 of its rows (M = 64: the
+//                   16-lane load shape, two rows per thread; M = 128: one row
+//                   per lane); the two warps of a quadrant swap their row
+//                   maxima through shared memory.  Online maximum in the log2
+//                   domain (O rescaled only when a row's maximum rises by more
+//                   than 8; the stale maximum is exact since the final
+//                   division uses the same one), P = 2^(x - m) as bf16 pairs
+//                   stored back over S[buf]
+//   O += P V        8 UMMA Mx128x16 with A = P in TMEM and B = the V page
 //                   (token rows, MN-major, both 64-column halves in one
 //                   instruction) -> TMEM O (fp32, 128 columns)
 // Warp 8 streams Q (3-D box per sequence) and the K pages, warp 10 the V pages
 // (two rings of 32 KB stages in the UMMA's 128B-swizzled layout, each stream
-// as far ahead as its own ring allows: three V stages, and three K stages when
-// the Q tile has at most 64 rows and takes 16 KB); warp 9 lane 0 issues the
-// UMMAs, QK of page i + 1 ahead of PV of page i so the tensor core overlaps
+// as far ahead as its own ring allows), both with the pages' buffers looked up
+// 32 to 64 pages ahead; warp 9 issues the UMMAs (one elected lane, four to a
+// burst), QK of page i + 1 ahead of PV of page i so the tensor core overlaps
 // the softmax (the last PV of a sequence is not held back).  TMEM: three S
 // buffers at columns 0, 128, 256 and O at 384.
 #pragma once

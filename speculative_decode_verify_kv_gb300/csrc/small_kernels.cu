@@ -1,7 +1,9 @@
 // small_kernels.cu -- the latency-bound kernels of the verify path:
 //   subpage_view_kernel   P128 page table -> P32 grouped-HND sub-page indices
-//   sparse_plan_kernel    per (request, KV head): unique selected blocks and
-//                         the bitmask of verify tokens that selected each
+//   zero_kernel           zeroes a call's counters inside the launch chain
+//   sparse_plan_kernel    per (request, KV head): unique selected blocks, the
+//                         bitmask of verify tokens that selected each, and
+//                         each block's page slot
 //   topk_kernel           warp-level per-token top-k (radix select), ties to
 //                         the lower block index, ascending output
 //   combine_kernel        split-KV combine: merges the (normalised output,
