@@ -407,42 +407,94 @@ def time_stage(name, steps, warmup):
 
 def time_e2e(name, steps, warmup):
     """Same step through the C ABI with host buffers: per step, H2D of q,
-    page table and kv_lens from pinned memory, the kernels, D2H of the output."""
+    page table and kv_lens from pinned memory, the kernels, D2H of the output.
+
+    Pipelined (the reported value): two sets of device buffers (one shared KV
+    pool); step i's copies run on a copy stream -- its inputs while step i - 1
+    computes, its output while step i + 1 computes -- and every step's copies
+    and kernels lie inside the timed region (events around the whole loop,
+    the compute stream joining the copy stream at the end).  Serial: the same
+    copies and kernels in order on one stream (reported beside it)."""
     import torch
     from speculative_decode_verify_kv_gb300.runtime import DeviceVerify
     p = make(name)
-    dv = DeviceVerify(p)
+    dvs = [DeviceVerify(p), DeviceVerify(p)]
+    dvs[1].pool = dvs[0].pool  # one resident KV pool
+    torch.cuda.empty_cache()
     hq = p.q.pin_memory()
     hpt = p.page_table.pin_memory()
     hl = p.kv_lens.pin_memory()
-    hout = torch.empty(dv.out.shape, dtype=dv.out.dtype).pin_memory()
+    houts = [torch.empty(dvs[0].out.shape, dtype=dvs[0].out.dtype).pin_memory() for _ in range(2)]
     msa = p.topk > 0
+    comp = torch.cuda.current_stream()
+    cs = torch.cuda.Stream()
+    E = lambda: torch.cuda.Event()  # noqa: E731
+    ev_in = [E(), E()]
+    ev_done = [E(), E()]
+    for e in ev_done:
+        e.record(comp)
 
-    def step():
-        dv.q.copy_(hq, non_blocking=True)
-        dv.page_table.copy_(hpt, non_blocking=True)
-        dv.kv_lens.copy_(hl, non_blocking=True)
+    def h2d(k, stream):
+        d = dvs[k]
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_done[k])  # the previous step on these buffers has finished
+            d.q.copy_(hq, non_blocking=True)
+            d.page_table.copy_(hpt, non_blocking=True)
+            d.kv_lens.copy_(hl, non_blocking=True)
+            ev_in[k].record(stream)
+
+    def kernels(k):
+        d = dvs[k]
+        comp.wait_event(ev_in[k])
         if msa:
-            dv.msa()
+            d.msa()
         else:
-            dv.subpage_view()
-            dv.dense()
-        hout.copy_(dv.out, non_blocking=True)
+            d.subpage_view()
+            d.dense()
+        ev_done[k].record(comp)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        step()
-    e.record()
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
-    h2d = hq.numel() * hq.element_size() + hpt.numel() * 4 + hl.numel() * 4
-    d2h = hout.numel() * hout.element_size()
-    return {"value": p.batch * p.qo_len / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    def d2h(k, stream):
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_done[k])
+            houts[k].copy_(dvs[k].out, non_blocking=True)
+
+    def pipelined(n):
+        h2d(0, cs)
+        for i in range(n):
+            k = i & 1
+            kernels(k)
+            if i + 1 < n:
+                h2d(k ^ 1, cs)
+            d2h(k, cs)
+        comp.wait_stream(cs)
+
+    def serial(n):
+        for i in range(n):
+            h2d(0, comp)
+            kernels(0)
+            d2h(0, comp)
+
+    out = {}
+    for label, run in (("pipelined", pipelined), ("serial", serial)):
+        run(warmup)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(comp)
+        cs.wait_stream(comp)
+        run(steps)
+        e.record(comp)
+        torch.cuda.synchronize()
+        out[label] = s.elapsed_time(e) / steps
+    ms = out["pipelined"]
+    h2d_b = hq.numel() * hq.element_size() + hpt.numel() * 4 + hl.numel() * 4
+    d2h_b = houts[0].numel() * houts[0].element_size()
+    res = {"value": p.batch * p.qo_len / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+           "h2d_bytes_per_step": int(h2d_b), "d2h_bytes_per_step": int(d2h_b),
+           "copies": "copy stream, double-buffered, overlapping the neighbouring steps' kernels",
+           "serial_value": p.batch * p.qo_len / (out["serial"] / 1e3), "serial_ms_per_step": out["serial"]}
+    del dvs
+    torch.cuda.empty_cache()
+    return res
 
 
 def cpu_baseline(name, budget_s=12.0):
@@ -676,6 +728,7 @@ def main():
     e2e = None if args.no_e2e else time_e2e(args.workload, max(10, args.steps // 4), args.warmup)
     if dist and e2e:
         e2e["value"] = job_value(qtok, world, max_over_ranks(e2e["ms_per_step"], dist))
+        e2e["serial_value"] = job_value(qtok, world, max_over_ranks(e2e["serial_ms_per_step"], dist))
 
     gbs = step_bytes / (ms / 1e3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -686,7 +739,9 @@ def main():
             "kv_hbm_gbs": sig(gbs), "kv_hbm_pct_of_measured_peak": sig(100 * gbs / peak),
             "kv_hbm_pct_of_nominal_8tbs": sig(100 * gbs / NOMINAL_HBM_GBS),
             "per_call_ms": {k: sig(v) for k, v in head["per_call_ms"].items()}, "roofline": roofline,
-            "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+            "e2e": ({k: (sig(e2e[k]) if k.endswith("value") else e2e[k])
+                     for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "copies",
+                               "serial_value")}
                     if e2e else None),
             "gpu_launches": head["launches_per_step"] * args.steps * head["repeats"],
             "clocks": clocks, "device_error": head["device_error"], "paths": summary}
